@@ -1,0 +1,385 @@
+"""Benchmark of the hot path: one step = AdaLN modulate + dense attention (head
+groups) + gated residual over one synthetic batch of the 10 s clip at
+1344x768 (72,576 tokens, 56 heads x 128, hidden 5,376).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fv|reference]
+
+Prints one JSON line.  ``value`` is attention TFLOP/s (4 N^2 d H per step over
+the whole step time, all ranks); ``roofline`` is the attention kernel's own
+rate against the measured bf16 peak; ``e2e`` times the same step through the
+C ABI with inputs copied from pinned host memory and results read back;
+``cpu_baseline`` times the fp64 oracle on a bounded sample of the step.
+``--impl reference`` times only that oracle (the slow reference arm).
+Under torchrun every rank runs its own copy of the workload (independent
+problems, no collective on the data path) and rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "attention TFLOP/s (4*N^2*d*H) at N=72,576, 56x128 heads; % of GB300 BF16 peak"
+UNIT = "TFLOP/s"
+EPS = 1e-6
+DATA = ("synthetic: seeded N(0,1) bf16 Q/K/V, residual x and branch output a; N(0,0.1^2) fp32 AdaLN tables "
+        "(8 steps, step 3); no trained weights")
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"bf16_tflops": d.get("bf16_tflops"), "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d.get("hbm_gbs"), "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value across ranks (the job's wall time is its slowest rank)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sample(w: W.Workload, q, k, v, x_mod, shift, scale, x_res, a, gate, rows_per_head: int):
+    """Run the fp64 oracle over a bounded sample of one step: the same
+    rows_per_head query rows of every head, and that many rows of the two
+    elementwise ops.  Returns (seconds, attention FLOPs of the sample)."""
+    import numpy as np
+
+    import oracle
+    sc = 1.0 / math.sqrt(W.HEAD_DIM)
+    t0 = time.perf_counter()
+    rows_e = np.arange(rows_per_head, dtype=np.int64) * max(1, w.n // max(1, rows_per_head))
+    oracle.modulate(x_mod, shift[W.ADALN_STEP].numpy(), scale[W.ADALN_STEP].numpy(), EPS, rows=rows_e)
+    outs = []
+    for h in range(w.heads):
+        rows = W.sampled_rows(w.n, h, rows_per_head).numpy()[:rows_per_head]
+        outs.append((h, rows, oracle.attn_rows(q, k, v, h, rows, sc)[0]))
+    oracle.gated_residual(x_res, a, gate[W.ADALN_STEP].numpy(), rows=rows_e)
+    dt = time.perf_counter() - t0
+    return dt, 4.0 * w.n * W.HEAD_DIM * rows_per_head * w.heads, outs
+
+
+def sample_errors(o_gpu: torch.Tensor, outs) -> dict:
+    """max-abs / mean-abs of the GPU output on the oracle's sampled rows."""
+    o_cpu = o_gpu.detach().cpu()
+    worst, tot, cnt = 0.0, 0.0, 0
+    for h, rows, ref in outs:
+        got = o_cpu[rows, h * W.HEAD_DIM:(h + 1) * W.HEAD_DIM].to(torch.float64).numpy()
+        d = abs(got - ref)
+        worst = max(worst, float(d.max()))
+        tot += float(d.sum())
+        cnt += d.size
+    return {"max_abs": worst, "mean_abs": tot / max(1, cnt), "rows": cnt // W.HEAD_DIM,
+            "pass": worst <= 2e-2 and tot / max(1, cnt) <= 2e-3}
+
+
+def cpu_inputs(w: W.Workload):
+    q, k, v = W.qkv(w)
+    x_mod, shift, scale = W.modulate_inputs(w, rows=w.n)
+    x_res, a, gate = W.gated_residual_inputs(w, rows=w.n)
+    return q, k, v, x_mod, shift, scale, x_res, a, gate
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle on the host cores, each step a
+    bounded sample of the workload, scaled to attention TFLOP/s."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = W.WORKLOADS[args.workload]
+    inputs = cpu_inputs(w)
+    rows = args.ref_rows
+    times = []
+    flops = 0.0
+    for i in range(args.warmup + args.steps):
+        dt, flops, _ = oracle_sample(w, *inputs, rows_per_head=rows)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = flops * len(times) / total / 1e12
+    cores = os.cpu_count()
+    sample = f"{rows} query rows of each of the {w.heads} heads (of {w.n}) + {rows} rows of modulate and gated residual"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w: W.Workload) -> dict:
+    groups = [min(w.head_group, w.heads - h0) for h0 in range(0, w.heads, w.head_group)]
+    return {"workload": w.name, "tokens": w.n, "heads": w.heads, "head_dim": W.HEAD_DIM,
+            "head_groups": groups, "hidden": W.HIDDEN, "adaln_step": W.ADALN_STEP,
+            "step": "adaln_modulate -> attention (head groups) -> gated_residual",
+            "l2": "inputs larger than L2 (5.3 GB resident working set vs 126 MB L2); no flush"}
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_fv(args):
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        from video_diffusion_transformer_gb300 import build as fbuild
+        fbuild.build()
+    barrier(world)
+    import video_diffusion_transformer_gb300 as fv
+    fv.load_library()
+
+    w = W.WORKLOADS[args.workload]
+    cpu = cpu_inputs(w)
+    q_h, k_h, v_h, xm_h, shift_h, scale_h, xr_h, a_h, gate_h = cpu
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    xm, xr, a = xm_h.to(dev), xr_h.to(dev), a_h.to(dev)
+    shift, scale, gate = shift_h.to(dev), scale_h.to(dev), gate_h.to(dev)
+    o = torch.empty_like(q)
+    y = torch.empty((w.n, W.HIDDEN), dtype=torch.bfloat16, device=dev)
+    out = torch.empty_like(xr)
+    stream = torch.cuda.Stream(device=dev)
+    launches_per_step = 1 + len(range(0, w.heads, w.head_group)) + 1
+
+    def step(ev0=None, ev1=None):
+        fv.adaln_modulate(xm, shift, scale, W.ADALN_STEP, eps=EPS, out=y, stream=stream)
+        if ev0 is not None:
+            ev0.record(stream)
+        fv.attn_fwd(q, k, v, o, head_group=w.head_group, stream=stream)
+        if ev1 is not None:
+            ev1.record(stream)
+        fv.gated_residual(xr, a, gate, W.ADALN_STEP, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        stream.synchronize()
+        fv.sync_status(stream)
+
+        # ---- device-resident timing
+        ev_a = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.3)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for i in range(args.steps):
+            step(*ev_a[i])
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        clocks = sampler.stop()
+        fv.sync_status(stream)
+        ms_total = start.elapsed_time(end)
+        attn_ms = [e0.elapsed_time(e1) for e0, e1 in ev_a]
+
+        # ---- end to end through the C ABI: pinned host inputs in, results out
+        e2e = None
+        if not args.no_e2e:
+            pin = [t.pin_memory() for t in (q_h, k_h, v_h, xm_h, xr_h, a_h)]
+            o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+            y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+            out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+            dsts = (q, k, v, xm, xr, a)
+            h2d = sum(t.numel() * t.element_size() for t in pin)
+            d2h = sum(t.numel() * t.element_size() for t in (o_h, y_h, out_h))
+
+            def e2e_step():
+                for d, s in zip(dsts, pin):
+                    d.copy_(s, non_blocking=True)
+                step()
+                o_h.copy_(o, non_blocking=True)
+                y_h.copy_(y, non_blocking=True)
+                out_h.copy_(out, non_blocking=True)
+
+            for _ in range(max(1, args.warmup // 2)):
+                e2e_step()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier(world)
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            for _ in range(args.steps):
+                e2e_step()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            barrier(world)
+            fv.sync_status(stream)
+            e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+            e2e = {"value": world * w.flops * args.steps / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                   "ms_per_step": e2e_ms / args.steps}
+
+    ms_total = max_over_ranks(ms_total, world, dev)
+
+    # CPU baseline: the oracle on a bounded sample of the step (rank 0, one GPU).
+    # Its attention rows double as a parity check of the output just timed.
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, fl, outs = oracle_sample(w, q_h, k_h, v_h, xm_h, shift_h, scale_h, xr_h, a_h, gate_h,
+                                     rows_per_head=args.cpu_rows)
+        cpu_baseline = {"value": fl / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                        "sample": f"{args.cpu_rows} query rows of each of the {w.heads} heads (of {w.n}) + "
+                                  f"{args.cpu_rows} rows of modulate and gated residual; {dt:.1f} s",
+                        "parity_of_timed_output": sample_errors(o, outs)}
+
+    if rank != 0:
+        return 0
+    pk = peaks()
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    achieved = w.flops / (attn_avg_ms / 1e3) / 1e12
+    peak = pk["bf16_tflops_sustained"]
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        traffic = json.load(open(prof)).get(w.name)
+    value = world * w.flops * args.steps / (ms_total / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": DATA, "config": config_of(w),
+        "pct_of_bf16_peak": {"burst": 100.0 * value / pk["bf16_tflops"] if pk["bf16_tflops"] else None,
+                             "sustained": 100.0 * value / peak if peak else None, "peaks": pk["source"]},
+        "roofline": {"kernel": "attn_fwd_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak if peak else None, "traffic": traffic,
+                     "peak_kind": f"bf16_tflops_sustained ({pk['source']})",
+                     "frac_of_burst": achieved / pk["bf16_tflops"] if pk["bf16_tflops"] else None,
+                     "per": f"one step's {len(range(0, w.heads, w.head_group))} head-group launches, "
+                            f"{w.flops / 1e12:.2f} TFLOP, avg {attn_avg_ms:.2f} ms"},
+        "e2e": e2e, "cpu_baseline": cpu_baseline, "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "elementwise_ms_per_step": (ms_total / args.steps) - attn_avg_ms,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def parse(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("fv", "reference"), default="fv")
+    ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--cpu-rows", type=int, default=96, help="oracle query rows per head for cpu_baseline")
+    ap.add_argument("--ref-rows", type=int, default=16, help="oracle query rows per head per reference step")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return args
+
+
+def main(argv=None):
+    args = parse(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_fv(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

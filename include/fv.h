@@ -1,0 +1,158 @@
+/*
+ * fv.h -- C ABI of the GB300 (sm_103a) dense video-token attention library.
+ *
+ * The library computes the hot path of one attention sub-layer of a
+ * MiniMax-H3-shaped video diffusion transformer block:
+ *
+ *   fv_adaln_modulate   y = LN(x) * (1 + scale[step]) + shift[step]
+ *   fv_attn_fwd         O = softmax(Q K^T * scale) V, full (unmasked), per head
+ *   fv_gated_residual   out = x + gate[step] * a
+ *
+ * Sources ("FreeVideo: a 66 GB video transformer on an 8 GB card"):
+ *   - section "What MiniMax H3 is, briefly": 56 heads of 128, Q/K/V 7168 wide,
+ *     hidden size 5,376, tokens = latent frames x (H/32) x (W/32);
+ *   - section "Why it does not fit: the arithmetic": the dense score matrix is
+ *     never materialised, flash-style kernels stream it; attention is the
+ *     time problem;
+ *   - section "Cut one: 26 GB of AdaLN weights become 0.22 GB of tables":
+ *     shift, scale and gate per step read from a stored table, and a call
+ *     whose timestep is not the stored one is an error;
+ *   - section "The rest is placement", item 1: attention runs on a group of
+ *     4, 8 or 16 of the 56 heads at a time; a slice is tokens x heads x 128 x 2
+ *     bytes.
+ * And "FastH3 Preview v1", section "Lever two: VSA-H3 ...": one joint
+ * bidirectional attention over the packed sequence (no causal mask).
+ *
+ * Conventions shared by every call:
+ *   - Ownership: the caller owns every buffer.  Device pointers are plain CUDA
+ *     device addresses (for example from torch).  The library allocates nothing
+ *     per call; it keeps one small device status word per device, allocated on
+ *     the first call that launches work on that device.
+ *   - Execution: every compute call only enqueues work on `stream` (a
+ *     cudaStream_t passed as void*; NULL is the legacy default stream) and
+ *     returns without synchronising.  Argument errors are detected on the host
+ *     before anything is enqueued.  Errors detected on the device (a bounded
+ *     wait that ran out) are recorded in the status word and returned by
+ *     fv_sync_status().
+ *   - Errors: the return value is a status code.  The library never aborts,
+ *     never exits and never traps a kernel.
+ *   - bfloat16 data is IEEE-like 1-8-7; every float32 -> bfloat16 conversion
+ *     rounds to nearest, ties to even.
+ */
+#ifndef FV_H
+#define FV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FV_OK = 0,
+    FV_ERR_NULL = -1,                /* a required pointer is NULL */
+    FV_ERR_SHAPE = -2,               /* a size is out of range (N < 1, D != 128, C % 8 != 0, ...) */
+    FV_ERR_ALIGN = -3,               /* a pointer or leading dimension breaks the 16-byte rule */
+    FV_ERR_STEP = -4,                /* step not in [0, num_steps), or timestep off the ladder */
+    FV_ERR_UNSUPPORTED_DEVICE = -5,  /* current device is not compute capability 10.3 */
+    FV_ERR_LAUNCH = -6,              /* a CUDA call or kernel launch failed */
+    FV_ERR_DEVICE_TIMEOUT = -7,      /* a bounded wait inside a kernel ran out */
+    FV_ERR_ARG = -8,                 /* a scalar argument is invalid (scale < 0, eps < 0, NaN, ...) */
+    FV_ERR_ALIAS = -9                /* buffers overlap where the call forbids it */
+} fv_status;
+
+/*
+ * Dense bidirectional attention forward over the packed video tokens.
+ *
+ * For every head h in [0, H) and query row i in [0, N):
+ *   s_ij = scale * q_i . k_j            (j = 0 .. N-1, no mask)
+ *   o_i  = sum_j exp(s_ij - m_i) v_j / sum_j exp(s_ij - m_i),  m_i = max_j s_ij
+ *   lse_i = m_i + ln sum_j exp(s_ij - m_i)
+ * computed tile by tile with an online softmax; the N x N scores never exist.
+ *
+ * Q, K, V, O: device, bfloat16, [N, H*D] row-major (token-major, row stride
+ *             H*D elements); head h occupies columns [h*D, h*D + D).  O must not
+ *             overlap Q, K or V.  Each base address 16-byte aligned.
+ * N:          tokens, >= 1 and < 2^31.
+ * H:          heads, 1 .. 256.
+ * D:          head dimension; must be 128.
+ * scale:      softmax scale, finite and >= 0 (1/sqrt(128) for the model).
+ * head_group: heads per launch, 1 .. H.  Heads run in groups of head_group
+ *             (the last group holds H mod head_group heads when that is
+ *             non-zero), one kernel launch per group, in order, on `stream`.
+ * lse:        optional device float32 [H, N] (row h holds head h), natural-log
+ *             log-sum-exp of each score row; NULL to skip.  4-byte aligned.
+ * stream:     cudaStream_t as void*.
+ * Compute: bf16 x bf16 products accumulated in float32 on the tensor cores;
+ * softmax in float32; probabilities rounded to bf16 for the P.V product;
+ * O normalised in float32 and rounded to bf16.
+ */
+fv_status fv_attn_fwd(const void *Q, const void *K, const void *V, void *O,
+                      int64_t N, int H, int D, float scale, int head_group,
+                      float *lse, void *stream);
+
+/*
+ * Cached-AdaLN modulated LayerNorm of the residual stream for one schedule step:
+ *   mu = mean_c x[i,c],  var = mean_c (x[i,c] - mu)^2   (biased)
+ *   y[i,c] = (x[i,c] - mu) / sqrt(var + eps) * (1 + scale_table[step*ld + c])
+ *            + shift_table[step*ld + c]
+ * The LayerNorm has no learned affine of its own; the table supplies it.
+ *
+ * x:            device bfloat16 [N, C] row-major, 16-byte aligned.
+ * y:            device [N, C]; float32 if y_is_fp32 != 0, else bfloat16.
+ *               16-byte aligned; must not overlap x.
+ * N:            rows (tokens), >= 1.   C: channels, 8 .. 8192, C % 8 == 0.
+ * shift_table, scale_table: device float32 [num_steps, table_ld]; row `step`
+ *               is read (each may be a strided view into a packed table of
+ *               several vectors).  16-byte aligned, table_ld >= C and
+ *               table_ld % 4 == 0.
+ * num_steps:    rows in the tables (>= 1).   step: 0 .. num_steps-1, else
+ *               FV_ERR_STEP (a timestep that is not on the stored schedule).
+ * eps:          >= 0 and finite.
+ */
+fv_status fv_adaln_modulate(const void *x, void *y, int y_is_fp32, int64_t N, int C,
+                            const float *shift_table, const float *scale_table,
+                            int64_t table_ld, int num_steps, int step, float eps,
+                            void *stream);
+
+/*
+ * Gated residual for one schedule step:
+ *   out[i,c] = x[i,c] + gate_table[step*ld + c] * a[i,c]
+ * computed as one float32 fused multiply-add, rounded once to bfloat16.
+ *
+ * x, a, out:  device bfloat16 [N, C] row-major, 16-byte aligned.  out may be
+ *             exactly x (in place); any other overlap is FV_ERR_ALIAS.
+ * gate_table: device float32 [num_steps, table_ld], 16-byte aligned,
+ *             table_ld >= C, table_ld % 4 == 0.
+ * N >= 1; C % 8 == 0, 8 .. 2^20; step in [0, num_steps) else FV_ERR_STEP.
+ */
+fv_status fv_gated_residual(const void *x, const void *a, void *out, int64_t N, int C,
+                            const float *gate_table, int64_t table_ld, int num_steps,
+                            int step, void *stream);
+
+/*
+ * Schedule cursor: the step whose stored timestep equals t exactly.
+ * ladder: host float32 [num_steps].  Writes the first matching index to
+ * *step_out and returns FV_OK, or returns FV_ERR_STEP if t is not on the
+ * ladder (the tables were computed for other timesteps).  Host only.
+ */
+fv_status fv_step_for_timestep(const float *ladder, int num_steps, float t, int *step_out);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's status word.
+ * Returns FV_OK, FV_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait
+ * since the last call, or FV_ERR_LAUNCH if the stream reports a CUDA error.
+ */
+fv_status fv_sync_status(void *stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *fv_status_string(fv_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FV_H */

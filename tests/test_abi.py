@@ -1,0 +1,126 @@
+"""The C-ABI library loads, exports every symbol include/fv.h declares, and
+rejects bad arguments on the host before touching a GPU.  No compute call
+runs here: every call below fails validation first (or is host-only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import video_diffusion_transformer_gb300 as fv
+from video_diffusion_transformer_gb300 import build as fbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fbuild.build()
+    return fv.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for need in ("fv_attn_fwd", "fv_adaln_modulate", "fv_gated_residual", "fv_step_for_timestep",
+                 "fv_sync_status", "fv_status_string"):
+        assert need in names
+    assert set(names) == set(fv.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.fv_version() >= 100
+
+
+def test_status_strings(lib):
+    for code, name in fv.STATUS.items():
+        assert fv.status_string(code).startswith(name)
+    assert fv.status_string(-123) == "unknown fv_status"
+
+
+def test_step_for_timestep():
+    ladder = [999.0, 749.0, 500.0, 250.0]
+    assert fv.step_for_timestep(ladder, 500.0) == 2
+    assert fv.step_for_timestep(ladder, 999.0) == 0
+    with pytest.raises(fv.FvError) as e:
+        fv.step_for_timestep(ladder, 501.0)
+    assert e.value.code == -4
+
+
+# Fake but well-aligned addresses: validation rejects every call below before
+# any CUDA call, so these are never dereferenced.
+A = 1 << 40
+B = A + (1 << 34)
+C = B + (1 << 34)
+O = C + (1 << 34)
+T = O + (1 << 34)
+
+
+def attn(lib, q=A, k=B, v=C, o=O, n=1008, h=4, d=128, scale=0.088, g=4, lse=None):
+    return lib.fv_attn_fwd(q, k, v, o, n, h, d, scale, g, lse, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(o=None), -1),
+    (dict(d=64), -2), (dict(n=0), -2), (dict(n=-5), -2), (dict(n=1 << 31), -2), (dict(h=0), -2),
+    (dict(h=257), -2), (dict(g=0), -2), (dict(g=5), -2),
+    (dict(scale=-1.0), -8), (dict(scale=float("nan")), -8), (dict(scale=float("inf")), -8),
+    (dict(q=A + 8), -3), (dict(o=O + 2), -3), (dict(lse=T + 2), -3),
+    (dict(o=A + 4096), -9), (dict(o=B), -9), (dict(lse=A + 64), -9),
+])
+def test_attn_rejects_bad_arguments(lib, kw, code):
+    assert attn(lib, **kw) == code
+
+
+def modulate(lib, x=A, y=O, fp32=0, n=1008, c=5376, sh=B, sc=C, ld=5376, steps=8, step=3, eps=1e-6):
+    return lib.fv_adaln_modulate(x, y, fp32, n, c, sh, sc, ld, steps, step, eps, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), -1), (dict(sh=None), -1),
+    (dict(n=0), -2), (dict(c=5377), -2), (dict(c=8200), -2), (dict(ld=5000), -2), (dict(steps=0), -2),
+    (dict(step=8), -4), (dict(step=-1), -4),
+    (dict(eps=-1e-6), -8), (dict(eps=float("nan")), -8),
+    (dict(x=A + 2), -3), (dict(sh=B + 4), -3), (dict(ld=5378), -3),
+    (dict(y=A + 1024), -9),
+])
+def test_modulate_rejects_bad_arguments(lib, kw, code):
+    assert modulate(lib, **kw) == code
+
+
+def gres(lib, x=A, a=B, out=O, n=5040, c=5376, g=C, ld=5376, steps=8, step=3):
+    return lib.fv_gated_residual(x, a, out, n, c, g, ld, steps, step, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(a=None), -1), (dict(g=None), -1),
+    (dict(n=0), -2), (dict(c=12), -2), (dict(ld=100), -2),
+    (dict(step=8), -4),
+    (dict(out=O + 8), -3), (dict(g=C + 4), -3),
+    (dict(out=B), -9), (dict(out=A + 16), -9),
+])
+def test_gated_residual_rejects_bad_arguments(lib, kw, code):
+    assert gres(lib, **kw) == code
+
+
+def test_python_binding_requires_cuda_tensors():
+    import torch
+    q = torch.zeros((128, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fv.attn_fwd(q, q, q)
+
+
+def test_product_package_never_imports_the_oracle():
+    pkg = os.path.dirname(fv.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cc", ".cpp")):
+                text = open(os.path.join(root, f)).read()
+                assert "oracle" not in text.lower(), f

@@ -1,0 +1,150 @@
+"""GPU parity of the AdaLN modulate and gated-residual kernels against the
+fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import video_diffusion_transformer_gb300 as fv
+import workloads as W
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+STEP = W.ADALN_STEP
+EPS = 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_ok):
+    from video_diffusion_transformer_gb300 import build
+    build.build()
+    fv.load_library()
+
+
+def check_modulate(x, shift, scale, rows, step=STEP, packed=None):
+    dev = torch.device("cuda")
+    xd = x.to(dev)
+    if packed is None:
+        sh_d, sc_d = shift.to(dev), scale.to(dev)
+    else:  # strided views into one packed [steps, vectors, C] table
+        sh_d, sc_d = packed
+    y32 = fv.adaln_modulate(xd, sh_d, sc_d, step, eps=EPS, out_dtype=torch.float32)
+    y16 = fv.adaln_modulate(xd, sh_d, sc_d, step, eps=EPS, out_dtype=torch.bfloat16)
+    fv.sync_status()
+    ref = oracle.modulate(x, shift[step].numpy(), scale[step].numpy(), EPS, rows=rows)
+    got32 = y32.cpu().numpy()[rows].astype(np.float64)
+    rel = np.abs(got32 - ref) / np.maximum(1.0, np.abs(ref))
+    assert rel.max() <= P.MODULATE_REL, rel.max()
+    # bf16 output: within one bf16 step of the oracle's value rounded once
+    ref16 = torch.from_numpy(ref).to(torch.bfloat16)
+    d = P.ulp_distance(P.bf16_bits(y16.cpu()[rows]), P.bf16_bits(ref16))
+    assert d.max() <= 1
+    got16 = y16.cpu()[rows].double().numpy()
+    assert np.abs(got16 - ref).max() <= P.MAX_ABS and np.abs(got16 - ref).mean() <= P.MEAN_ABS
+
+
+def test_modulate_tiny_all_rows():
+    w = W.WORKLOADS["tiny_1008"]
+    x, shift, scale = W.modulate_inputs(w)
+    check_modulate(x, shift, scale, np.arange(w.n))
+
+
+@pytest.mark.parametrize("name", ["clip10s_72576", "clip14s_102816"])
+def test_modulate_full_size_sampled_rows(name):
+    w = W.WORKLOADS[name]
+    x, shift, scale = W.modulate_inputs(w)
+    rows = np.unique(np.concatenate([np.arange(0, w.n, 97), [w.n - 1]]))
+    check_modulate(x, shift, scale, rows)
+
+
+def test_modulate_reads_strided_rows_of_a_packed_table():
+    """Six vectors per step packed as [steps, 6, C] (shift, scale, gate for
+    attention, then for the feed-forward); the call reads two strided views."""
+    c, steps = W.HIDDEN, 8
+    g = torch.Generator().manual_seed(5)
+    packed = (torch.randn((steps, 6, c), generator=g) * 0.1).to(torch.float32)
+    x = W.randn_bf16((300, c), 9, "x")
+    dev = torch.device("cuda")
+    pd = packed.to(dev)
+    shift_view, scale_view = pd[:, 0, :], pd[:, 1, :]
+    assert shift_view.stride(0) == 6 * c
+    for step in (0, 5, 7):
+        check_modulate(x, packed[:, 0, :].contiguous(), packed[:, 1, :].contiguous(), np.arange(300), step=step,
+                       packed=(shift_view, scale_view))
+
+
+@pytest.mark.parametrize("c", [8, 256, 1000, 2048, 4096, 5376, 8192])
+def test_modulate_other_widths(c):
+    x = W.randn_bf16((77, c), 3, "x")
+    g = torch.Generator().manual_seed(c)
+    shift = (torch.randn((4, c), generator=g) * 0.1).float()
+    scale = (torch.randn((4, c), generator=g) * 0.1).float()
+    check_modulate(x, shift, scale, np.arange(77), step=2)
+
+
+def test_modulate_constant_row_gives_shift():
+    c = W.HIDDEN
+    x = torch.full((4, c), 1.5, dtype=torch.bfloat16)
+    shift = W.adaln_table(0, "shift")
+    scale = W.adaln_table(0, "scale")
+    y = fv.adaln_modulate(x.cuda(), shift.cuda(), scale.cuda(), STEP, out_dtype=torch.float32).cpu()
+    assert torch.equal(y, shift[STEP].expand(4, c))
+
+
+def check_gres(x, a, gate, rows, step=STEP, in_place=False):
+    dev = torch.device("cuda")
+    xd, ad = x.to(dev), a.to(dev)
+    out = fv.gated_residual(xd, ad, gate.to(dev), step, out=xd if in_place else None)
+    fv.sync_status()
+    _, ref_bits = oracle.gated_residual(x, a, gate[step].numpy(), rows=rows)
+    d = P.ulp_distance(P.bf16_bits(out.cpu()[rows]), ref_bits)
+    assert d.max() <= 1
+    return int((d == 1).sum()), d.size
+
+
+def test_gated_residual_all_rows():
+    w = W.WORKLOADS["clip17_5040"]
+    x, a, gate = W.gated_residual_inputs(w)
+    ones, total = check_gres(x, a, gate, np.arange(w.n))
+    print(f"gated residual: {ones} of {total} elements one bf16 step from the oracle")
+    assert ones <= total * 1e-3
+
+
+def test_gated_residual_in_place():
+    w = W.WORKLOADS["clip17_5040"]
+    x, a, gate = W.gated_residual_inputs(w, rows=1000)
+    check_gres(x, a, gate, np.arange(1000), in_place=True)
+
+
+@pytest.mark.parametrize("name", ["clip10s_72576", "clip14s_102816"])
+def test_gated_residual_full_size_sampled_rows(name):
+    w = W.WORKLOADS[name]
+    x, a, gate = W.gated_residual_inputs(w)
+    rows = np.unique(np.concatenate([np.arange(0, w.n, 61), [w.n - 1]]))
+    check_gres(x, a, gate, rows)
+
+
+@pytest.mark.parametrize("c", [8, 264, 2056, 6000])
+def test_gated_residual_other_widths(c):
+    x = W.randn_bf16((33, c), 4, "x")
+    a = W.randn_bf16((33, c), 4, "a")
+    gate = (torch.randn((2, c), generator=torch.Generator().manual_seed(c)) * 0.1).float()
+    check_gres(x, a, gate, np.arange(33), step=1)
+
+
+def test_zero_gate_is_identity():
+    w = W.WORKLOADS["clip17_5040"]
+    x, a, _ = W.gated_residual_inputs(w, rows=64)
+    gate = torch.zeros((8, W.HIDDEN), dtype=torch.float32)
+    out = fv.gated_residual(x.cuda(), a.cuda(), gate.cuda(), STEP).cpu()
+    assert np.array_equal(P.bf16_bits(out), P.bf16_bits(x))
+
+
+def test_off_ladder_step_is_rejected():
+    x = torch.zeros((8, 64), dtype=torch.bfloat16, device="cuda")
+    gate = torch.zeros((8, 64), dtype=torch.float32, device="cuda")
+    with pytest.raises(fv.FvError) as e:
+        fv.gated_residual(x, x.clone(), gate, 8)
+    assert e.value.code == -4
+    with pytest.raises(fv.FvError):
+        fv.adaln_modulate(x, gate, gate, -1)

@@ -1,0 +1,174 @@
+"""Python binding of the GB300 dense video-token attention library.
+
+Argument marshalling only: every step of the path runs in the CUDA kernels of
+``_build/libfv.so`` (built from ``csrc/`` by ``build.py``), called through its
+C ABI (``include/fv.h``) with ctypes.  torch supplies device memory and the
+current stream.  There is no fallback: if the library is missing or the GPU
+is not compute capability 10.3, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfv.so")
+
+STATUS = {
+    0: "FV_OK", -1: "FV_ERR_NULL", -2: "FV_ERR_SHAPE", -3: "FV_ERR_ALIGN", -4: "FV_ERR_STEP",
+    -5: "FV_ERR_UNSUPPORTED_DEVICE", -6: "FV_ERR_LAUNCH", -7: "FV_ERR_DEVICE_TIMEOUT", -8: "FV_ERR_ARG",
+    -9: "FV_ERR_ALIAS",
+}
+# every symbol include/fv.h declares
+EXPORTS = ("fv_attn_fwd", "fv_adaln_modulate", "fv_gated_residual", "fv_step_for_timestep", "fv_sync_status",
+           "fv_status_string", "fv_version")
+
+HEAD_DIM = 128
+DEFAULT_SCALE = 1.0 / math.sqrt(HEAD_DIM)
+
+
+class FvError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)}")
+
+
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load the C-ABI library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"libfv.so not built ({p}); run video_diffusion_transformer_gb300/build.py "
+                          "or __graft_entry__.build()")
+    lib = ctypes.CDLL(p)
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    lib.fv_attn_fwd.argtypes = [vp, vp, vp, vp, i64, i32, i32, f32, i32, vp, vp]
+    lib.fv_attn_fwd.restype = i32
+    lib.fv_adaln_modulate.argtypes = [vp, vp, i32, i64, i32, vp, vp, i64, i32, i32, f32, vp]
+    lib.fv_adaln_modulate.restype = i32
+    lib.fv_gated_residual.argtypes = [vp, vp, vp, i64, i32, vp, i64, i32, i32, vp]
+    lib.fv_gated_residual.restype = i32
+    lib.fv_step_for_timestep.argtypes = [ctypes.POINTER(ctypes.c_float), i32, f32, ctypes.POINTER(ctypes.c_int)]
+    lib.fv_step_for_timestep.restype = i32
+    lib.fv_sync_status.argtypes = [vp]
+    lib.fv_sync_status.restype = i32
+    lib.fv_status_string.argtypes = [i32]
+    lib.fv_status_string.restype = ctypes.c_char_p
+    lib.fv_version.argtypes = []
+    lib.fv_version.restype = i32
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load_library().fv_status_string(int(code)).decode()
+    except ImportError:
+        return STATUS.get(int(code), f"status {code}")
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise FvError(code, where)
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor | None = None, *,
+             heads: int | None = None, head_group: int = 16, scale: float = DEFAULT_SCALE,
+             lse: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """O = softmax(Q K^T * scale) V per head, no mask.
+
+    q, k, v: bf16 CUDA [N, H*128] (token-major) or [N, H, 128]; returns O of the
+    same shape.  lse: optional float32 [H, N] filled with the log-sum-exp.
+    """
+    n = q.shape[0]
+    width = q.numel() // max(1, n)
+    h = heads if heads is not None else width // HEAD_DIM
+    if h * HEAD_DIM != width or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [N, H*128]")
+    if out is None:
+        out = torch.empty_like(q)
+    ptrs = [_dev(t, nm, torch.bfloat16) for t, nm in ((q, "q"), (k, "k"), (v, "v"), (out, "out"))]
+    lse_ptr = None
+    if lse is not None:
+        if lse.shape != (h, n):
+            raise ValueError("lse must be float32 [H, N]")
+        lse_ptr = _dev(lse, "lse", torch.float32)
+    code = load_library().fv_attn_fwd(*ptrs, n, h, HEAD_DIM, float(scale), int(min(head_group, h)), lse_ptr,
+                                      _stream_ptr(stream))
+    _check(code, "fv_attn_fwd")
+    return out
+
+
+def adaln_modulate(x: torch.Tensor, shift_table: torch.Tensor, scale_table: torch.Tensor, step: int, *,
+                   eps: float = 1e-6, out: torch.Tensor | None = None, out_dtype=torch.bfloat16,
+                   stream=None) -> torch.Tensor:
+    """y = LN(x) * (1 + scale_table[step]) + shift_table[step]; x bf16 [N, C], tables float32 [steps, C]."""
+    n, c = x.shape
+    if out is None:
+        out = torch.empty((n, c), dtype=out_dtype, device=x.device)
+    if shift_table.shape != scale_table.shape or shift_table.dim() != 2:
+        raise ValueError("tables must be float32 [steps, ld]")
+    for t, nm in ((shift_table, "shift_table"), (scale_table, "scale_table")):
+        if t.stride(1) != 1:
+            raise ValueError(f"{nm} rows must be contiguous")
+    if out.dtype not in (torch.bfloat16, torch.float32) or out.shape != (n, c):
+        raise ValueError("out must be bfloat16 or float32 [N, C]")
+    code = load_library().fv_adaln_modulate(
+        _dev(x, "x", torch.bfloat16), _dev(out, "out", out.dtype), 1 if out.dtype == torch.float32 else 0, n, c,
+        shift_table.data_ptr(), scale_table.data_ptr(), shift_table.stride(0), shift_table.shape[0], int(step),
+        float(eps), _stream_ptr(stream))
+    _check(code, "fv_adaln_modulate")
+    return out
+
+
+def gated_residual(x: torch.Tensor, a: torch.Tensor, gate_table: torch.Tensor, step: int, *,
+                   out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out = x + gate_table[step] * a (bf16 [N, C]); out may be x itself."""
+    n, c = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    if gate_table.dim() != 2 or gate_table.stride(1) != 1:
+        raise ValueError("gate_table must be float32 [steps, ld] with contiguous rows")
+    code = load_library().fv_gated_residual(
+        _dev(x, "x", torch.bfloat16), _dev(a, "a", torch.bfloat16), _dev(out, "out", torch.bfloat16), n, c,
+        gate_table.data_ptr(), gate_table.stride(0), gate_table.shape[0], int(step), _stream_ptr(stream))
+    _check(code, "fv_gated_residual")
+    return out
+
+
+def step_for_timestep(ladder, t: float) -> int:
+    """Index of timestep t on the stored ladder; raises FvError(FV_ERR_STEP) if absent."""
+    arr = (ctypes.c_float * len(ladder))(*[float(v) for v in ladder])
+    out = ctypes.c_int(-1)
+    _check(load_library().fv_step_for_timestep(arr, len(ladder), float(t), ctypes.byref(out)),
+           "fv_step_for_timestep")
+    return out.value
+
+
+def sync_status(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel recorded a device-side error."""
+    _check(load_library().fv_sync_status(_stream_ptr(stream)), "fv_sync_status")

@@ -1,0 +1,507 @@
+// Dense bidirectional softmax attention forward for sm_103a (GB300).
+//
+// Computes, for every head h of a launch and every query row i,
+//   o_i = sum_j exp(s_ij - m_i) v_j / sum_j exp(s_ij - m_i),  s_ij = scale q_i.k_j,
+// over all N keys with no mask: the full attention over the packed video tokens
+// of "FreeVideo: a 66 GB video transformer on an 8 GB card" (section "What
+// MiniMax H3 is, briefly": 56 heads of 128; section "Why it does not fit: the
+// arithmetic": the N x N scores are streamed, never stored).  Heads are
+// launched in groups (section "The rest is placement", item 1).
+//
+// Design (one persistent CTA per SM, 320 threads):
+//   * work unit = (head, block of 256 query rows) = two 128-row q-tiles;
+//     units are dealt round-robin, heads outermost, so the CTAs running at
+//     the same time stream the same head's K/V through L2;
+//   * warp 8 (one thread) issues TMA loads: the two Q tiles of a unit, then
+//     K_0, V_0, K_1, V_1, ... into a 4-slot ring of 32 KB tiles, each tile two
+//     128 x 64 bf16 halves in the 128-byte swizzled layout;
+//   * warp 9 (one thread) issues tcgen05 MMAs: S_k = Q_k K_j^T (both operands
+//     K-major in shared memory) and O_k += P_k V_j (P from tensor memory, V
+//     MN-major in shared memory), ping-ponging between the two q-tiles so the
+//     tensor core works on one tile while the other tile's softmax runs;
+//   * warps 0-3 and 4-7 are the softmax warpgroups of q-tile 0 and 1: thread
+//     t owns query row t (TMEM lane t).  Per K/V tile it reads its 128 scores
+//     from TMEM, takes the row maximum, writes p = 2^(s*scale*log2e - m) as
+//     bf16 back over the scores, and adds p to its float32 row sum.  The
+//     running maximum is raised (and O rescaled in TMEM) only when the tile
+//     maximum exceeds it by more than 2^8, so rescaling is rare;
+//   * TMEM (512 columns): S_0, S_1 at columns 0 and 128, O_0, O_1 at 256 and
+//     384, each 128 lanes x 128 float32 columns.  P_k (bf16 pairs) overwrites
+//     the first 64 columns of S_k.
+// All waits are bounded (see sm103_ptx.cuh); a wait that runs out records
+// kDevTimeout | where in the status word and the CTA drains and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "fv_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fv {
+namespace {
+
+constexpr int kD = 128;              // head dimension
+constexpr int kRows = 128;           // rows of a Q tile and of a K/V tile
+constexpr int kQTiles = 2;           // q-tiles per work unit
+constexpr int kUnitRows = kQTiles * kRows;
+constexpr int kStages = 4;           // K/V ring slots
+constexpr int kHalfBytes = kRows * 64 * 2;   // one 128 x 64 bf16 half tile (16 KB)
+constexpr int kTileBytes = 2 * kHalfBytes;   // 32 KB
+constexpr int kSoftmaxWarps = 4 * kQTiles;
+constexpr int kTmaWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;    // log2 units
+
+// barrier indices
+constexpr int kBarKvFull = 0;
+constexpr int kBarKvEmpty = kBarKvFull + kStages;
+constexpr int kBarQFull = kBarKvEmpty + kStages;
+constexpr int kBarQEmpty = kBarQFull + 1;
+constexpr int kBarSFull = kBarQEmpty + 1;
+constexpr int kBarPFull = kBarSFull + kQTiles;
+constexpr int kBarOFull = kBarPFull + kQTiles;
+constexpr int kBarDrain = kBarOFull + kQTiles;
+constexpr int kNumBars = kBarDrain + 1;
+
+// shared memory layout, offsets from a 1024-byte aligned base
+constexpr int kSmemQ = 0;
+constexpr int kSmemKV = kSmemQ + kQTiles * kTileBytes;
+constexpr int kSmemBar = kSmemKV + kStages * kTileBytes;
+constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
+constexpr int kSmemUsed = kSmemMisc + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for the 1024-byte alignment
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+// where codes for the status word
+constexpr int kWhereQEmpty = 1, kWhereKvEmpty = 2, kWhereQFull = 3, kWhereKvFull = 4, kWherePFull = 5,
+              kWhereSFull = 6, kWhereOFull = 7, kWhereDrain = 8;
+
+struct Params {
+    __nv_bfloat16 *o;
+    float *lse;
+    int *status;
+    int n;           // tokens
+    int ld;          // row stride of Q/K/V/O in elements (H * 128)
+    int head_begin;  // first head of this launch
+    int q_blocks;    // ceil(n / 256)
+    int kv_tiles;    // ceil(n / 128)
+    int num_units;   // heads * q_blocks
+    float scale_log2;  // scale * log2(e)
+};
+
+struct Smem {
+    uint32_t q, kv, bar;
+    volatile int *abort_flag;
+    __device__ uint32_t b(int i) const { return bar + 8u * (uint32_t)i; }
+};
+
+__device__ __forceinline__ bool wait_bar(const Smem &sm, int i, uint32_t parity, const Params &p, int where) {
+    return ptx::mbar_wait(sm.b(i), parity, sm.abort_flag, p.status, kDevTimeout | where);
+}
+
+// Wait used while draining: ignores the abort flag, still bounded in time.
+__device__ __forceinline__ void drain_bar(const Smem &sm, int i, uint32_t parity, const Params &p) {
+    int never = 0;
+    ptx::mbar_wait(sm.b(i), parity, &never, p.status, kDevTimeout | kWhereDrain);
+}
+
+// ------------------------------------------------------------------ TMA
+__device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv, const Params &p,
+                         const Smem &sm) {
+    uint32_t loads = 0;     // K/V tiles issued into the ring
+    uint32_t q_loads = 0;   // Q pairs issued
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
+        const int head = p.head_begin + unit / p.q_blocks;
+        const int qb = unit % p.q_blocks;
+        const int x0 = head * kD;
+        ok = wait_bar(sm, kBarQEmpty, (q_loads & 1u) ^ 1u, p, kWhereQEmpty);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(sm.b(kBarQFull), kQTiles * kTileBytes);
+        for (int k = 0; k < kQTiles; ++k) {
+            const int y = qb * kUnitRows + k * kRows;
+            const uint32_t dst = sm.q + (uint32_t)(k * kTileBytes);
+            ptx::tma_load_2d(dst, tq, sm.b(kBarQFull), x0, y);
+            ptx::tma_load_2d(dst + kHalfBytes, tq, sm.b(kBarQFull), x0 + 64, y);
+        }
+        ++q_loads;
+        for (int j = 0; ok && j < p.kv_tiles; ++j) {
+            for (int w = 0; w < 2; ++w) {
+                const uint32_t s = loads % kStages, ph = (loads / kStages) & 1u;
+                ok = wait_bar(sm, kBarKvEmpty + (int)s, ph ^ 1u, p, kWhereKvEmpty);
+                if (!ok) break;
+                ptx::mbar_arrive_expect_tx(sm.b(kBarKvFull + (int)s), kTileBytes);
+                const CUtensorMap *m = w ? tv : tk;
+                const uint32_t dst = sm.kv + s * (uint32_t)kTileBytes;
+                ptx::tma_load_2d(dst, m, sm.b(kBarKvFull + (int)s), x0, j * kRows);
+                ptx::tma_load_2d(dst + kHalfBytes, m, sm.b(kBarKvFull + (int)s), x0 + 64, j * kRows);
+                ++loads;
+            }
+        }
+    }
+    // Before the CTA exits, every copy it started must have landed.
+    for (uint32_t s = 0; s < (uint32_t)kStages && s < loads; ++s) {
+        const uint32_t last = ((loads - 1u - s) / kStages) * kStages + s;
+        drain_bar(sm, kBarKvFull + (int)s, (last / kStages) & 1u, p);
+    }
+    if (q_loads > 0) drain_bar(sm, kBarQFull, (q_loads - 1u) & 1u, p);
+}
+
+// ------------------------------------------------------------------ MMA
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_tile, uint32_t k_tile) {
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = (uint32_t)((kk >> 2) * kHalfBytes + (kk & 3) * 32);
+        const uint64_t a = ptx::sdesc_sw128(q_tile + off, 16, 1024);
+        const uint64_t b = ptx::sdesc_sw128(k_tile + off, 16, 1024);
+        ptx::mma_ss(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_tile, bool accumulate) {
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, true);
+#pragma unroll
+    for (int kk = 0; kk < kRows / 16; ++kk) {
+        // 16 keys per MMA: 16 rows of 128 bytes; the next 64 dims sit in the
+        // other half tile (leading offset 16 KB), 8-key groups are 1 KB apart.
+        const uint64_t b = ptx::sdesc_sw128(v_tile + (uint32_t)(kk * 16 * 128), kHalfBytes, 1024);
+        ptx::mma_ts(d_tmem, p_tmem + (uint32_t)(kk * 8), b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+__device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
+    uint32_t ring = 0;   // ring index of K_0 of the current unit
+    uint32_t tile = 0;   // K/V tiles finished (same count for every q-tile)
+    uint32_t units = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
+        ok = wait_bar(sm, kBarQFull, units & 1u, p, kWhereQFull);
+        if (!ok) break;
+        {
+            const uint32_t s = ring % kStages;
+            ok = wait_bar(sm, kBarKvFull + (int)s, (ring / kStages) & 1u, p, kWhereKvFull);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            for (int k = 0; k < kQTiles; ++k) {
+                issue_qk(tmem + (uint32_t)(128 * k), sm.q + (uint32_t)(k * kTileBytes),
+                         sm.kv + s * (uint32_t)kTileBytes);
+                ptx::tc_commit(sm.b(kBarSFull + k));
+            }
+            ptx::tc_commit(sm.b(kBarKvEmpty + (int)s));
+        }
+        for (int j = 0; ok && j < p.kv_tiles; ++j) {
+            const uint32_t iv = ring + 2u * (uint32_t)j + 1u, sv = iv % kStages;
+            const uint32_t ik = iv + 1u, sk = ik % kStages;
+            const bool more = j + 1 < p.kv_tiles;
+            ok = wait_bar(sm, kBarKvFull + (int)sv, (iv / kStages) & 1u, p, kWhereKvFull);
+            if (!ok) break;
+            for (int k = 0; k < kQTiles; ++k) {
+                ok = wait_bar(sm, kBarPFull + k, tile & 1u, p, kWherePFull);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                issue_pv(tmem + 256u + (uint32_t)(128 * k), tmem + (uint32_t)(128 * k),
+                         sm.kv + sv * (uint32_t)kTileBytes, j > 0);
+                if (k == kQTiles - 1) ptx::tc_commit(sm.b(kBarKvEmpty + (int)sv));
+                if (!more) ptx::tc_commit(sm.b(kBarOFull + k));
+                if (more) {
+                    if (k == 0) {
+                        ok = wait_bar(sm, kBarKvFull + (int)sk, (ik / kStages) & 1u, p, kWhereKvFull);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                    }
+                    issue_qk(tmem + (uint32_t)(128 * k), sm.q + (uint32_t)(k * kTileBytes),
+                             sm.kv + sk * (uint32_t)kTileBytes);
+                    ptx::tc_commit(sm.b(kBarSFull + k));
+                    if (k == kQTiles - 1) ptx::tc_commit(sm.b(kBarKvEmpty + (int)sk));
+                }
+            }
+            ++tile;
+        }
+        if (!ok) break;
+        ptx::tc_commit(sm.b(kBarQEmpty));
+        ring += 2u * (uint32_t)p.kv_tiles;
+        ++units;
+    }
+    // Every MMA issued must complete before the tensor memory is released.
+    ptx::tc_commit(sm.b(kBarDrain));
+    drain_bar(sm, kBarDrain, 0u, p);
+}
+
+// -------------------------------------------------------------- softmax
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Row maximum of the 128 raw scores; columns >= valid are ignored.
+template <bool kMasked>
+__device__ __forceinline__ float row_max(const uint32_t (&s)[4][32], int valid) {
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            const int c = c4 * 32 + i;
+            if (!kMasked || c < valid) m0 = fmaxf(m0, u2f(s[c4][i]));
+            if (!kMasked || c + 1 < valid) m1 = fmaxf(m1, u2f(s[c4][i + 1]));
+        }
+    return fmaxf(m0, m1);
+}
+
+// p = 2^(s * scale_log2 - m) rounded to bf16 pairs and stored over the first
+// 64 columns of S; returns the float32 sum of p.
+template <bool kMasked>
+__device__ __forceinline__ float write_probs(const uint32_t (&s)[4][32], int valid, float scale_log2, float m,
+                                             uint32_t t_s) {
+    float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c4l = 0; c4l < 2; ++c4l) {
+            const int c4 = half * 2 + c4l;
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const int c = c4 * 32 + i;
+                float p0 = ptx::ex2_approx(fmaf(u2f(s[c4][i]), scale_log2, -m));
+                float p1 = ptx::ex2_approx(fmaf(u2f(s[c4][i + 1]), scale_log2, -m));
+                if (kMasked) {
+                    p0 = c < valid ? p0 : 0.f;
+                    p1 = c + 1 < valid ? p1 : 0.f;
+                }
+                sum0 += p0;
+                sum1 += p1;
+                pk[c4l * 16 + i / 2] = pack_bf16x2(p0, p1);
+            }
+        }
+        ptx::tmem_st_32x32b_x32(t_s + (uint32_t)(half * 32), pk);
+    }
+    return sum0 + sum1;
+}
+
+__device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int k, int t) {
+    const uint32_t lane_base = (uint32_t)((t >> 5) * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + (uint32_t)(128 * k);
+    const uint32_t t_o = tmem + lane_base + 256u + (uint32_t)(128 * k);
+    uint32_t tile = 0, units = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
+        const int head = p.head_begin + unit / p.q_blocks;
+        const int row = (unit % p.q_blocks) * kUnitRows + k * kRows + t;
+        float m_used = -INFINITY, l = 0.f;
+        for (int j = 0; j < p.kv_tiles; ++j) {
+            ok = __all_sync(0xffffffffu, wait_bar(sm, kBarSFull + k, tile & 1u, p, kWhereSFull));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            uint32_t s[4][32];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) ptx::tmem_ld_32x32b_x32(t_s + (uint32_t)(32 * c4), s[c4]);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) ptx::reg_fence(s[c4]);
+            const int valid = p.n - j * kRows;
+            const bool masked = valid < kRows;
+            const float m_tile = (masked ? row_max<true>(s, valid) : row_max<false>(s, valid)) * p.scale_log2;
+            float factor = 1.f;
+            bool rescale = false;
+            if (j == 0) {
+                m_used = m_tile;
+            } else if (m_tile > m_used + kRescaleThreshold) {
+                factor = ptx::ex2_approx(m_used - m_tile);
+                m_used = m_tile;
+                rescale = true;
+            }
+            const float tile_sum = masked ? write_probs<true>(s, valid, p.scale_log2, m_used, t_s)
+                                          : write_probs<false>(s, valid, p.scale_log2, m_used, t_s);
+            l = l * factor + tile_sum;
+            // O (complete through tile j-1, since S_j is) must carry the new maximum
+            // before the next P.V accumulates into it.
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t o[32];
+                    ptx::tmem_ld_32x32b_x32(t_o + (uint32_t)(32 * c4), o);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence(o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * factor);
+                    ptx::tmem_st_32x32b_x32(t_o + (uint32_t)(32 * c4), o);
+                }
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(sm.b(kBarPFull + k));
+            ++tile;
+        }
+        if (!ok) break;
+        ok = __all_sync(0xffffffffu, wait_bar(sm, kBarOFull + k, units & 1u, p, kWhereOFull));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const float inv_l = 1.0f / l;
+        const bool row_ok = row < p.n;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(row_ok ? row : 0) * (size_t)p.ld + (size_t)head * kD);
+#pragma unroll 1
+        for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t o[32];
+            ptx::tmem_ld_32x32b_x32(t_o + (uint32_t)(32 * c4), o);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence(o);
+            if (row_ok) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint4 w;
+                    w.x = pack_bf16x2(u2f(o[8 * v + 0]) * inv_l, u2f(o[8 * v + 1]) * inv_l);
+                    w.y = pack_bf16x2(u2f(o[8 * v + 2]) * inv_l, u2f(o[8 * v + 3]) * inv_l);
+                    w.z = pack_bf16x2(u2f(o[8 * v + 4]) * inv_l, u2f(o[8 * v + 5]) * inv_l);
+                    w.w = pack_bf16x2(u2f(o[8 * v + 6]) * inv_l, u2f(o[8 * v + 7]) * inv_l);
+                    dst[c4 * 4 + v] = w;
+                }
+            }
+        }
+        if (p.lse != nullptr && row_ok)
+            p.lse[(size_t)head * (size_t)p.n + (size_t)row] = (m_used + log2f(l)) * 0.69314718055994531f;
+        ++units;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    Smem sm;
+    sm.q = base + kSmemQ;
+    sm.kv = base + kSmemKV;
+    sm.bar = base + kSmemBar;
+    sm.abort_flag = reinterpret_cast<volatile int *>(smem + kSmemMisc + 4);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + kSmemMisc);
+
+    const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(sm.b(kBarKvFull + s), 1);
+            ptx::mbar_init(sm.b(kBarKvEmpty + s), 1);
+        }
+        ptx::mbar_init(sm.b(kBarQFull), 1);
+        ptx::mbar_init(sm.b(kBarQEmpty), 1);
+        for (int k = 0; k < kQTiles; ++k) {
+            ptx::mbar_init(sm.b(kBarSFull + k), 1);
+            ptx::mbar_init(sm.b(kBarPFull + k), 128);
+            ptx::mbar_init(sm.b(kBarOFull + k), 1);
+        }
+        ptx::mbar_init(sm.b(kBarDrain), 1);
+        *sm.abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kTmaWarp && lane == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
+
+    if (warp == kTmaWarp) {
+        if (lane == 0) producer(&tm_q, &tm_k, &tm_v, p, sm);
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) mma_issuer(p, sm, tmem);
+    } else {
+        softmax_role(p, sm, tmem, warp >> 2, (int)threadIdx.x & 127);
+    }
+    __syncwarp();  // lanes 1-31 of the TMA and MMA warps wait here for lane 0
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// -------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// [n, ld] bf16 row-major, boxes of 128 rows x 64 columns, 128-byte swizzle,
+// zero fill outside the tensor.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t n, int ld) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)n};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2u};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)kRows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+fv_status launch_attn_fwd(const AttnLaunch &a, cudaStream_t stream) {
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FV_ERR_LAUNCH;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+                cudaSuccess)
+                return FV_ERR_LAUNCH;
+            attr_set[dev] = true;
+        }
+    }
+    const int ld = a.heads_total * kD;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, a.q, a.n, ld) || !make_map(&mk, a.k, a.n, ld) || !make_map(&mv, a.v, a.n, ld))
+        return FV_ERR_LAUNCH;
+    Params p;
+    p.o = static_cast<__nv_bfloat16 *>(a.o);
+    p.lse = a.lse;
+    p.status = a.status;
+    p.n = (int)a.n;
+    p.ld = ld;
+    p.head_begin = a.head_begin;
+    p.q_blocks = (int)((a.n + kUnitRows - 1) / kUnitRows);
+    p.kv_tiles = (int)((a.n + kRows - 1) / kRows);
+    p.num_units = a.heads * p.q_blocks;
+    p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
+    const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
+    attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
+}
+
+}  // namespace fv

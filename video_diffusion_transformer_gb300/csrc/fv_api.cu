@@ -1,0 +1,193 @@
+// C ABI of the library (declared in include/fv.h): argument checks on the
+// host, device checks, the per-device status word, and head-group launches.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fv.h"
+#include "fv_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool probed = false;
+    bool supported = false;
+    int num_sms = 0;
+    int *status = nullptr;  // device int, zeroed at allocation
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// Current device's state; probes compute capability and SM count, and
+// allocates the status word, on first use.
+fv_status device_state(DeviceState **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FV_ERR_LAUNCH;
+    std::lock_guard<std::mutex> g(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FV_ERR_LAUNCH;
+        d.supported = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        d.probed = true;
+    }
+    if (!d.supported) return FV_ERR_UNSUPPORTED_DEVICE;
+    if (d.status == nullptr) {
+        void *p = nullptr;
+        if (cudaMalloc(&p, 256) != cudaSuccess) return FV_ERR_LAUNCH;
+        if (cudaMemset(p, 0, 256) != cudaSuccess) {
+            cudaFree(p);
+            return FV_ERR_LAUNCH;
+        }
+        d.status = static_cast<int *>(p);
+    }
+    *out = &d;
+    return FV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fv_status fv_attn_fwd(const void *Q, const void *K, const void *V, void *O, int64_t N, int H, int D, float scale,
+                      int head_group, float *lse, void *stream) {
+    if (!Q || !K || !V || !O) return FV_ERR_NULL;
+    if (D != 128 || N < 1 || N >= (int64_t(1) << 31) || H < 1 || H > 256 || head_group < 1 || head_group > H)
+        return FV_ERR_SHAPE;
+    if (!std::isfinite(scale) || scale < 0.0f) return FV_ERR_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || (lse && !aligned(lse, 4)))
+        return FV_ERR_ALIGN;
+    const size_t bytes = (size_t)N * (size_t)H * 128u * 2u;
+    if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
+        return FV_ERR_ALIAS;
+    if (lse) {
+        const size_t lb = (size_t)N * (size_t)H * 4u;
+        if (overlaps(lse, lb, O, bytes) || overlaps(lse, lb, Q, bytes) || overlaps(lse, lb, K, bytes) ||
+            overlaps(lse, lb, V, bytes))
+            return FV_ERR_ALIAS;
+    }
+    DeviceState *d = nullptr;
+    fv_status st = device_state(&d);
+    if (st != FV_OK) return st;
+    fv::AttnLaunch a;
+    a.q = Q;
+    a.k = K;
+    a.v = V;
+    a.o = O;
+    a.lse = lse;
+    a.n = N;
+    a.heads_total = H;
+    a.scale = scale;
+    a.status = d->status;
+    a.num_sms = d->num_sms;
+    for (int h0 = 0; h0 < H; h0 += head_group) {
+        a.head_begin = h0;
+        a.heads = (H - h0) < head_group ? (H - h0) : head_group;
+        st = fv::launch_attn_fwd(a, static_cast<cudaStream_t>(stream));
+        if (st != FV_OK) return st;
+    }
+    return FV_OK;
+}
+
+fv_status fv_adaln_modulate(const void *x, void *y, int y_is_fp32, int64_t N, int C, const float *shift_table,
+                            const float *scale_table, int64_t table_ld, int num_steps, int step, float eps,
+                            void *stream) {
+    if (!x || !y || !shift_table || !scale_table) return FV_ERR_NULL;
+    if (N < 1 || C < 8 || C > 8192 || (C % 8) != 0 || table_ld < C || num_steps < 1) return FV_ERR_SHAPE;
+    if (step < 0 || step >= num_steps) return FV_ERR_STEP;
+    if (!std::isfinite(eps) || eps < 0.0f) return FV_ERR_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(shift_table, 16) || !aligned(scale_table, 16) ||
+        (table_ld % 4) != 0)
+        return FV_ERR_ALIGN;
+    const size_t xb = (size_t)N * (size_t)C * 2u, yb = (size_t)N * (size_t)C * (y_is_fp32 ? 4u : 2u);
+    if (overlaps(x, xb, y, yb)) return FV_ERR_ALIAS;
+    DeviceState *d = nullptr;
+    fv_status st = device_state(&d);
+    if (st != FV_OK) return st;
+    return fv::launch_adaln_modulate(x, y, y_is_fp32 != 0, N, C, shift_table + (int64_t)step * table_ld,
+                                     scale_table + (int64_t)step * table_ld, eps, d->num_sms,
+                                     static_cast<cudaStream_t>(stream));
+}
+
+fv_status fv_gated_residual(const void *x, const void *a, void *out, int64_t N, int C, const float *gate_table,
+                            int64_t table_ld, int num_steps, int step, void *stream) {
+    if (!x || !a || !out || !gate_table) return FV_ERR_NULL;
+    if (N < 1 || C < 8 || C > (1 << 20) || (C % 8) != 0 || table_ld < C || num_steps < 1) return FV_ERR_SHAPE;
+    if (step < 0 || step >= num_steps) return FV_ERR_STEP;
+    if (!aligned(x, 16) || !aligned(a, 16) || !aligned(out, 16) || !aligned(gate_table, 16) || (table_ld % 4) != 0)
+        return FV_ERR_ALIGN;
+    const size_t b = (size_t)N * (size_t)C * 2u;
+    if (overlaps(out, b, a, b)) return FV_ERR_ALIAS;
+    if (out != x && overlaps(out, b, x, b)) return FV_ERR_ALIAS;
+    DeviceState *d = nullptr;
+    fv_status st = device_state(&d);
+    if (st != FV_OK) return st;
+    return fv::launch_gated_residual(x, a, out, N, C, gate_table + (int64_t)step * table_ld, d->num_sms,
+                                     static_cast<cudaStream_t>(stream));
+}
+
+fv_status fv_step_for_timestep(const float *ladder, int num_steps, float t, int *step_out) {
+    if (!ladder || !step_out) return FV_ERR_NULL;
+    if (num_steps < 1) return FV_ERR_SHAPE;
+    for (int i = 0; i < num_steps; ++i) {
+        if (ladder[i] == t) {
+            *step_out = i;
+            return FV_OK;
+        }
+    }
+    return FV_ERR_STEP;
+}
+
+fv_status fv_sync_status(void *stream) {
+    DeviceState *d = nullptr;
+    fv_status st = device_state(&d);
+    if (st != FV_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FV_ERR_LAUNCH;
+    int word = 0;
+    if (cudaMemcpyAsync(&word, d->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return FV_ERR_LAUNCH;
+    if (word != 0) {
+        if (cudaMemsetAsync(d->status, 0, sizeof(int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+            return FV_ERR_LAUNCH;
+        return FV_ERR_DEVICE_TIMEOUT;
+    }
+    return FV_OK;
+}
+
+const char *fv_status_string(fv_status s) {
+    switch (s) {
+        case FV_OK: return "FV_OK";
+        case FV_ERR_NULL: return "FV_ERR_NULL: a required pointer is NULL";
+        case FV_ERR_SHAPE: return "FV_ERR_SHAPE: a size is out of range";
+        case FV_ERR_ALIGN: return "FV_ERR_ALIGN: a pointer or leading dimension is not 16-byte aligned";
+        case FV_ERR_STEP: return "FV_ERR_STEP: step/timestep is not on the stored schedule";
+        case FV_ERR_UNSUPPORTED_DEVICE: return "FV_ERR_UNSUPPORTED_DEVICE: needs a compute capability 10.3 GPU";
+        case FV_ERR_LAUNCH: return "FV_ERR_LAUNCH: a CUDA call or kernel launch failed";
+        case FV_ERR_DEVICE_TIMEOUT: return "FV_ERR_DEVICE_TIMEOUT: a bounded wait inside a kernel ran out";
+        case FV_ERR_ARG: return "FV_ERR_ARG: a scalar argument is invalid";
+        case FV_ERR_ALIAS: return "FV_ERR_ALIAS: buffers overlap where the call forbids it";
+    }
+    return "unknown fv_status";
+}
+
+int fv_version(void) { return 100; }
+
+}  // extern "C"

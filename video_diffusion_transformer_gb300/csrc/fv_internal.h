@@ -1,0 +1,37 @@
+// Internal declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "fv.h"
+
+namespace fv {
+
+// Device status word values (0 = no error).  A kernel that gives up on a
+// bounded wait stores kDevTimeout | where, where names the wait.
+constexpr int kDevTimeout = 0x7100;
+
+struct AttnLaunch {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;
+    int64_t n;
+    int heads_total;   // H (row stride of Q/K/V/O is H * 128)
+    int head_begin;    // first head of this launch
+    int heads;         // heads in this launch
+    float scale;
+    int *status;       // device status word
+    int num_sms;
+};
+
+// Enqueue one head-group launch of the attention kernel.
+fv_status launch_attn_fwd(const AttnLaunch &a, cudaStream_t stream);
+
+fv_status launch_adaln_modulate(const void *x, void *y, bool y_fp32, int64_t n, int c, const float *shift_row,
+                                const float *scale_row, float eps, int num_sms, cudaStream_t stream);
+
+fv_status launch_gated_residual(const void *x, const void *a, void *out, int64_t n, int c, const float *gate_row,
+                                int num_sms, cudaStream_t stream);
+
+}  // namespace fv
