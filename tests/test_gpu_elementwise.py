@@ -35,11 +35,13 @@ def check_modulate(x, shift, scale, rows, step=STEP, packed=None):
     got32 = y32.cpu().numpy()[rows].astype(np.float64)
     rel = np.abs(got32 - ref) / np.maximum(1.0, np.abs(ref))
     assert rel.max() <= P.MODULATE_REL, rel.max()
-    # bf16 output: within one bf16 step of the oracle's value rounded once
-    ref16 = torch.from_numpy(ref).to(torch.bfloat16)
-    d = P.ulp_distance(P.bf16_bits(y16.cpu()[rows]), P.bf16_bits(ref16))
-    assert d.max() <= 1
+    # bf16 output: the bf16 rounding of a value within the float32 tolerance,
+    # i.e. |y16 - y| <= half a bf16 step of y + 1e-5 * max(|y|, 1).  (Where y
+    # is near zero by cancellation, that can be several bf16 steps of y.)
     got16 = y16.cpu()[rows].double().numpy()
+    half_step = np.where(ref != 0, np.exp2(np.floor(np.log2(np.abs(ref) + 1e-300)) - 8), 0.0)
+    bound = half_step + P.MODULATE_REL * np.maximum(1.0, np.abs(ref))
+    assert np.all(np.abs(got16 - ref) <= bound), float(np.max(np.abs(got16 - ref) - bound))
     assert np.abs(got16 - ref).max() <= P.MAX_ABS and np.abs(got16 - ref).mean() <= P.MEAN_ABS
 
 
