@@ -145,6 +145,40 @@ fv_status fv_step_for_timestep(const float *ladder, int num_steps, float t, int 
  */
 fv_status fv_sync_status(void *stream);
 
+/*
+ * fv_attn_fwd for callers that must not allocate device memory.  The pages
+ * have no counterpart: this is a property of the library, not of the method.
+ *
+ * fv_attn_fwd allocates (once per device, with cudaMalloc) the small status
+ * word its kernels report into.  A caller whose device memory is owned by
+ * someone else -- a framework's caching allocator, or a serving process that
+ * budgets every byte of a fixed pool -- cannot let a library call cudaMalloc
+ * behind its back, and cudaMalloc can also synchronise the whole device.
+ * This variant computes exactly what fv_attn_fwd computes, with the same
+ * arguments and checks, but keeps its scratch (one status word per
+ * head-group launch) in an array compiled into the library: it calls no
+ * cudaMalloc, cudaFree or other allocating routine.  The caller still passes
+ * all inputs and outputs.
+ *
+ * Limits and sharing:
+ *   - at most FV_NOALLOC_MAX_LAUNCHES head-group launches per call, i.e.
+ *     ceil(H / head_group) <= 64; a call needing more returns FV_ERR_SHAPE
+ *     before doing anything;
+ *   - the scratch array is one per device and shared by every call on that
+ *     device; each call clears the words it uses (on `stream`) before its
+ *     launches.  Calls whose work overlaps on the GPU (different streams, or
+ *     different host threads without ordering) race on it: order them;
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ * device_status_out: NULL to return right after enqueueing (device-side
+ *   timeouts then go unreported); otherwise the call synchronises `stream`,
+ *   then writes FV_OK or FV_ERR_DEVICE_TIMEOUT to *device_status_out.
+ */
+#define FV_NOALLOC_MAX_LAUNCHES 64
+fv_status fv_attn_fwd_noalloc(const void *Q, const void *K, const void *V, void *O,
+                              int64_t N, int H, int D, float scale, int head_group,
+                              float *lse, void *stream, int *device_status_out);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *fv_status_string(fv_status s);
 

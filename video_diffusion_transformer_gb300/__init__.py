@@ -24,7 +24,8 @@ STATUS = {
 }
 # every symbol include/fv.h declares
 EXPORTS = ("fv_attn_fwd", "fv_adaln_modulate", "fv_gated_residual", "fv_step_for_timestep", "fv_sync_status",
-           "fv_status_string", "fv_version")
+           "fv_status_string", "fv_version", "fv_attn_fwd_noalloc")
+NOALLOC_MAX_LAUNCHES = 64
 
 HEAD_DIM = 128
 DEFAULT_SCALE = 1.0 / math.sqrt(HEAD_DIM)
@@ -64,6 +65,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fv_status_string.restype = ctypes.c_char_p
     lib.fv_version.argtypes = []
     lib.fv_version.restype = i32
+    lib.fv_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, i64, i32, i32, f32, i32, vp, vp, ctypes.POINTER(ctypes.c_int)]
+    lib.fv_attn_fwd_noalloc.restype = i32
     if path is None:
         _lib = lib
     return lib
@@ -120,6 +123,39 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tenso
     code = load_library().fv_attn_fwd(*ptrs, n, h, HEAD_DIM, float(scale), int(min(head_group, h)), lse_ptr,
                                       _stream_ptr(stream))
     _check(code, "fv_attn_fwd")
+    return out
+
+
+def attn_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor | None = None, *,
+                     heads: int | None = None, head_group: int = 16, scale: float = DEFAULT_SCALE,
+                     lse: torch.Tensor | None = None, stream=None, check_device_status: bool = True) -> torch.Tensor:
+    """attn_fwd without any device allocation by the library (fv_attn_fwd_noalloc).
+
+    For callers whose device memory belongs to a pool they manage: the
+    library's scratch lives in a fixed array compiled into it.  At most
+    NOALLOC_MAX_LAUNCHES head-group launches per call.  With
+    check_device_status the call waits for the stream and raises on a
+    device-side timeout.
+    """
+    n = q.shape[0]
+    width = q.numel() // max(1, n)
+    h = heads if heads is not None else width // HEAD_DIM
+    if h * HEAD_DIM != width or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [N, H*128]")
+    if out is None:
+        out = torch.empty_like(q)
+    ptrs = [_dev(t, nm, torch.bfloat16) for t, nm in ((q, "q"), (k, "k"), (v, "v"), (out, "out"))]
+    lse_ptr = None
+    if lse is not None:
+        if lse.shape != (h, n):
+            raise ValueError("lse must be float32 [H, N]")
+        lse_ptr = _dev(lse, "lse", torch.float32)
+    dev_status = ctypes.c_int(0)
+    code = load_library().fv_attn_fwd_noalloc(*ptrs, n, h, HEAD_DIM, float(scale), int(min(head_group, h)), lse_ptr,
+                                              _stream_ptr(stream),
+                                              ctypes.byref(dev_status) if check_device_status else None)
+    _check(code, "fv_attn_fwd_noalloc")
+    _check(dev_status.value, "fv_attn_fwd_noalloc (device)")
     return out
 
 
