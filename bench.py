@@ -49,6 +49,16 @@ def peaks() -> dict:
     return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def attn_source_hash() -> str:
+    """Hash of the attention kernel's sources; ties recorded ncu traffic to them."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("attn_fwd.cu", "sm103_ptx.cuh"):
+        with open(os.path.join(ROOT, "video_diffusion_transformer_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -332,7 +342,9 @@ def run_fv(args):
     traffic = None
     prof = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(prof):
-        traffic = json.load(open(prof)).get(w.name)
+        rec = json.load(open(prof)).get(w.name)
+        if rec and rec.get("kernel_source") == attn_source_hash():
+            traffic = rec["attn_fwd_kernel_bytes_per_step"]
     value = world * w.flops * args.steps / (ms_total / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -245,47 +245,60 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // Row maximum of the 128 raw scores; columns >= valid are ignored.
 template <bool kMasked>
 __device__ __forceinline__ float row_max(const uint32_t (&s)[4][32], int valid) {
-    float m0 = -INFINITY, m1 = -INFINITY;
+    if (!kMasked) {
+        // two independent chains of three-input maxima
+        float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                m0 = ptx::max3(m0, u2f(s[c4][i]), u2f(s[c4][i + 1]));
+                m1 = ptx::max3(m1, u2f(s[c4][i + 2]), u2f(s[c4][i + 3]));
+            }
+        return fmaxf(m0, m1);
+    }
+    float m = -INFINITY;
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-            const int c = c4 * 32 + i;
-            if (!kMasked || c < valid) m0 = fmaxf(m0, u2f(s[c4][i]));
-            if (!kMasked || c + 1 < valid) m1 = fmaxf(m1, u2f(s[c4][i + 1]));
-        }
-    return fmaxf(m0, m1);
+        for (int i = 0; i < 32; ++i)
+            if (c4 * 32 + i < valid) m = fmaxf(m, u2f(s[c4][i]));
+    return m;
 }
 
 // p = 2^(s * scale_log2 - m) rounded to bf16 pairs and stored over the first
-// 64 columns of S; returns the float32 sum of p.
+// 64 columns of S; returns the float32 sum of p.  Pairs of columns share one
+// packed multiply-add and one packed add.
 template <bool kMasked>
 __device__ __forceinline__ float write_probs(const uint32_t (&s)[4][32], int valid, float scale_log2, float m,
                                              uint32_t t_s) {
-    float sum0 = 0.f, sum1 = 0.f;
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+    for (int c4 = 0; c4 < 4; ++c4) {
+        // 32 scores -> 16 packed bf16 pairs -> P columns [16 c4, 16 c4 + 16)
+        uint32_t pk[16];
 #pragma unroll
-        for (int c4l = 0; c4l < 2; ++c4l) {
-            const int c4 = half * 2 + c4l;
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const int c = c4 * 32 + i;
-                float p0 = ptx::ex2_approx(fmaf(u2f(s[c4][i]), scale_log2, -m));
-                float p1 = ptx::ex2_approx(fmaf(u2f(s[c4][i + 1]), scale_log2, -m));
-                if (kMasked) {
-                    p0 = c < valid ? p0 : 0.f;
-                    p1 = c + 1 < valid ? p1 : 0.f;
-                }
-                sum0 += p0;
-                sum1 += p1;
-                pk[c4l * 16 + i / 2] = pack_bf16x2(p0, p1);
+        for (int i = 0; i < 32; i += 4) {
+            const int c = c4 * 32 + i;
+            float x0, x1, x2, x3;
+            ptx::fma2(x0, x1, u2f(s[c4][i]), u2f(s[c4][i + 1]), scale_log2, -m);
+            ptx::fma2(x2, x3, u2f(s[c4][i + 2]), u2f(s[c4][i + 3]), scale_log2, -m);
+            float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
+            float p2 = ptx::ex2_approx(x2), p3 = ptx::ex2_approx(x3);
+            if (kMasked) {
+                p0 = c < valid ? p0 : 0.f;
+                p1 = c + 1 < valid ? p1 : 0.f;
+                p2 = c + 2 < valid ? p2 : 0.f;
+                p3 = c + 3 < valid ? p3 : 0.f;
             }
+            ptx::add2(a0, a1, p0, p1);
+            ptx::add2(b0, b1, p2, p3);
+            pk[i / 2] = pack_bf16x2(p0, p1);
+            pk[i / 2 + 1] = pack_bf16x2(p2, p3);
         }
-        ptx::tmem_st_32x32b_x32(t_s + (uint32_t)(half * 32), pk);
+        ptx::tmem_st_32x32b_x16(t_s + (uint32_t)(c4 * 16), pk);
     }
-    return sum0 + sum1;
+    return (a0 + a1) + (b0 + b1);
 }
 
 __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int k, int t) {

@@ -31,6 +31,20 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
     f[4] = bf_lo(v.z); f[5] = bf_hi(v.z); f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
 }
 
+// The same unpacking, but opaque to common-subexpression elimination: a row
+// is unpacked afresh in each of its three passes, so only the packed row
+// (4 registers per chunk) stays live between passes.
+__device__ __forceinline__ void unpack8_fresh(const uint4 &v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t lo, hi;
+        asm volatile("shl.b32 %0, %2, 16;\n\tand.b32 %1, %2, 0xffff0000;" : "=r"(lo), "=r"(hi) : "r"(w[i]));
+        f[2 * i] = __uint_as_float(lo);
+        f[2 * i + 1] = __uint_as_float(hi);
+    }
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -38,14 +52,14 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // y = LN(x) * (1 + scale_row) + shift_row.  kChunks = 16-byte chunks per lane
-// per row (ceil(C / 256)); a row stays in registers between the two
-// reductions (mean, then mean of squared deviations) and the output pass.
+// per row (ceil(C / 256)); the packed bf16 row stays in registers between the
+// two reductions (mean, then mean of squared deviations) and the output pass,
+// which keeps the kernel at 125 registers: two 256-thread CTAs per SM.
 // Shared memory holds the step's table rows: shift[C], then 1 + scale[C].
 template <int kChunks>
-__global__ void __launch_bounds__(kEwThreads) modulate_kernel(const uint4 *__restrict__ x, void *__restrict__ y,
-                                                              int y_fp32, int64_t n, int c,
-                                                              const float *__restrict__ shift_row,
-                                                              const float *__restrict__ scale_row, float eps) {
+__global__ void __launch_bounds__(kEwThreads, kChunks <= 21 ? 2 : 1)
+    modulate_kernel(const uint4 *__restrict__ x, void *__restrict__ y, int y_fp32, int64_t n, int c,
+                    const float *__restrict__ shift_row, const float *__restrict__ scale_row, float eps) {
     extern __shared__ float4 tab4[];
     float *tab = reinterpret_cast<float *>(tab4);
     for (int i = (int)threadIdx.x; i < c; i += kEwThreads) {
@@ -70,7 +84,7 @@ __global__ void __launch_bounds__(kEwThreads) modulate_kernel(const uint4 *__res
 #pragma unroll
         for (int i = 0; i < kChunks; ++i) {
             float f[8];
-            unpack8(v[i], f);
+            unpack8_fresh(v[i], f);
 #pragma unroll
             for (int e = 0; e < 8; ++e) s += f[e];
         }
@@ -80,7 +94,7 @@ __global__ void __launch_bounds__(kEwThreads) modulate_kernel(const uint4 *__res
         for (int i = 0; i < kChunks; ++i) {
             if (lane + 32 * i < cq) {
                 float f[8];
-                unpack8(v[i], f);
+                unpack8_fresh(v[i], f);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const float d = f[e] - mu;
@@ -94,7 +108,7 @@ __global__ void __launch_bounds__(kEwThreads) modulate_kernel(const uint4 *__res
             const int q = lane + 32 * i;
             if (q < cq) {
                 float f[8];
-                unpack8(v[i], f);
+                unpack8_fresh(v[i], f);
                 const float4 a0 = sh4[2 * q], a1 = sh4[2 * q + 1];
                 const float4 b0 = sc4[2 * q], b1 = sc4[2 * q + 1];
                 const float sh[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
