@@ -153,29 +153,45 @@ __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUt
 }
 
 // ------------------------------------------------------------------ MMA
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_tile, uint32_t k_tile) {
+// One thread issues every MMA, so its scalar work per instruction bounds the
+// tensor pipe: descriptors are built once per CTA and each instruction only
+// adds a compile-time offset to the 14-bit start-address field (addresses stay
+// below 256 KB, so the field never carries).
+struct MmaDescs {
+    uint64_t q0;   // Q tile 0, K-major, 128-byte swizzle
+    uint64_t kv0;  // ring slot 0 read as a K-major operand (K tiles)
+    uint64_t v0;   // ring slot 0 read as an MN-major operand (V tiles)
+};
+
+constexpr uint64_t kDescTile = (uint64_t)(kTileBytes >> 4);  // one 32 KB tile in descriptor units
+
+// S = Q K^T: 8 MMAs of M = N = 128, K = 16, both operands K-major.
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
     constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
 #pragma unroll
     for (int kk = 0; kk < kD / 16; ++kk) {
-        const uint32_t off = (uint32_t)((kk >> 2) * kHalfBytes + (kk & 3) * 32);
-        const uint64_t a = ptx::sdesc_sw128(q_tile + off, 16, 1024);
-        const uint64_t b = ptx::sdesc_sw128(k_tile + off, 16, 1024);
-        ptx::mma_ss(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
+        const uint64_t off = (uint64_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+        ptx::mma_ss(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
     }
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_tile, bool accumulate) {
+// O (+)= P V: 8 MMAs; P (bf16 pairs) from tensor memory, V MN-major: 16 keys
+// per MMA are 16 rows of 128 bytes; the second 64 dims sit in the other half
+// tile (leading offset 16 KB), 8-key groups are 1 KB apart (stride offset).
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc, bool accumulate) {
     constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, true);
 #pragma unroll
     for (int kk = 0; kk < kRows / 16; ++kk) {
-        // 16 keys per MMA: 16 rows of 128 bytes; the next 64 dims sit in the
-        // other half tile (leading offset 16 KB), 8-key groups are 1 KB apart.
-        const uint64_t b = ptx::sdesc_sw128(v_tile + (uint32_t)(kk * 16 * 128), kHalfBytes, 1024);
-        ptx::mma_ts(d_tmem, p_tmem + (uint32_t)(kk * 8), b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+        const uint64_t off = (uint64_t)((kk * 16 * 128) >> 4);
+        ptx::mma_ts(d_tmem, p_tmem + (uint32_t)(kk * 8), v_desc + off, idesc, (accumulate || kk > 0) ? 1u : 0u);
     }
 }
 
 __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
+    MmaDescs dsc;
+    dsc.q0 = ptx::sdesc_sw128(sm.q, 16, 1024);
+    dsc.kv0 = ptx::sdesc_sw128(sm.kv, 16, 1024);
+    dsc.v0 = ptx::sdesc_sw128(sm.kv, kHalfBytes, 1024);
     uint32_t ring = 0;   // ring index of K_0 of the current unit
     uint32_t tile = 0;   // K/V tiles finished (same count for every q-tile)
     uint32_t units = 0;
@@ -188,9 +204,10 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
             ok = wait_bar(sm, kBarKvFull + (int)s, (ring / kStages) & 1u, p, kWhereKvFull);
             if (!ok) break;
             ptx::tc_fence_after();
+            const uint64_t kdesc = dsc.kv0 + s * kDescTile;
+#pragma unroll
             for (int k = 0; k < kQTiles; ++k) {
-                issue_qk(tmem + (uint32_t)(128 * k), sm.q + (uint32_t)(k * kTileBytes),
-                         sm.kv + s * (uint32_t)kTileBytes);
+                issue_qk(tmem + (uint32_t)(128 * k), dsc.q0 + (uint64_t)k * kDescTile, kdesc);
                 ptx::tc_commit(sm.b(kBarSFull + k));
             }
             ptx::tc_commit(sm.b(kBarKvEmpty + (int)s));
@@ -201,12 +218,14 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
             const bool more = j + 1 < p.kv_tiles;
             ok = wait_bar(sm, kBarKvFull + (int)sv, (iv / kStages) & 1u, p, kWhereKvFull);
             if (!ok) break;
+            const uint64_t vdesc = dsc.v0 + sv * kDescTile;
+            const uint64_t kdesc = dsc.kv0 + sk * kDescTile;
+#pragma unroll
             for (int k = 0; k < kQTiles; ++k) {
                 ok = wait_bar(sm, kBarPFull + k, tile & 1u, p, kWherePFull);
                 if (!ok) break;
                 ptx::tc_fence_after();
-                issue_pv(tmem + 256u + (uint32_t)(128 * k), tmem + (uint32_t)(128 * k),
-                         sm.kv + sv * (uint32_t)kTileBytes, j > 0);
+                issue_pv(tmem + 256u + (uint32_t)(128 * k), tmem + (uint32_t)(128 * k), vdesc, j > 0);
                 if (k == kQTiles - 1) ptx::tc_commit(sm.b(kBarKvEmpty + (int)sv));
                 if (!more) ptx::tc_commit(sm.b(kBarOFull + k));
                 if (more) {
@@ -215,8 +234,7 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
                         if (!ok) break;
                         ptx::tc_fence_after();
                     }
-                    issue_qk(tmem + (uint32_t)(128 * k), sm.q + (uint32_t)(k * kTileBytes),
-                             sm.kv + sk * (uint32_t)kTileBytes);
+                    issue_qk(tmem + (uint32_t)(128 * k), dsc.q0 + (uint64_t)k * kDescTile, kdesc);
                     ptx::tc_commit(sm.b(kBarSFull + k));
                     if (k == kQTiles - 1) ptx::tc_commit(sm.b(kBarKvEmpty + (int)sk));
                 }
