@@ -35,6 +35,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 
 #include "fv_internal.h"
@@ -92,6 +93,7 @@ struct Params {
     int kv_tiles;    // ceil(n / 128)
     int num_units;   // heads * q_blocks
     float scale_log2;  // scale * log2(e)
+    int skip_load;     // test hook: CTA 0 never issues its K/V load number skip_load (-1: off)
 };
 
 struct Smem {
@@ -115,6 +117,9 @@ __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUt
                          const Smem &sm) {
     uint32_t loads = 0;     // K/V tiles issued into the ring
     uint32_t q_loads = 0;   // Q pairs issued
+    // Test hook: a load that is never issued, so that the consumer's bounded
+    // wait runs out.  Such a load must not be waited for below.
+    const int64_t skipped = blockIdx.x == 0 ? (int64_t)p.skip_load : -1;
     bool ok = true;
     for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
         const int head = p.head_begin + unit / p.q_blocks;
@@ -135,11 +140,13 @@ __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUt
                 const uint32_t s = loads % kStages, ph = (loads / kStages) & 1u;
                 ok = wait_bar(sm, kBarKvEmpty + (int)s, ph ^ 1u, p, kWhereKvEmpty);
                 if (!ok) break;
-                ptx::mbar_arrive_expect_tx(sm.b(kBarKvFull + (int)s), kTileBytes);
-                const CUtensorMap *m = w ? tv : tk;
-                const uint32_t dst = sm.kv + s * (uint32_t)kTileBytes;
-                ptx::tma_load_2d(dst, m, sm.b(kBarKvFull + (int)s), x0, j * kRows);
-                ptx::tma_load_2d(dst + kHalfBytes, m, sm.b(kBarKvFull + (int)s), x0 + 64, j * kRows);
+                if ((int64_t)loads != skipped) {
+                    ptx::mbar_arrive_expect_tx(sm.b(kBarKvFull + (int)s), kTileBytes);
+                    const CUtensorMap *m = w ? tv : tk;
+                    const uint32_t dst = sm.kv + s * (uint32_t)kTileBytes;
+                    ptx::tma_load_2d(dst, m, sm.b(kBarKvFull + (int)s), x0, j * kRows);
+                    ptx::tma_load_2d(dst + kHalfBytes, m, sm.b(kBarKvFull + (int)s), x0 + 64, j * kRows);
+                }
                 ++loads;
             }
         }
@@ -147,7 +154,7 @@ __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUt
     // Before the CTA exits, every copy it started must have landed.
     for (uint32_t s = 0; s < (uint32_t)kStages && s < loads; ++s) {
         const uint32_t last = ((loads - 1u - s) / kStages) * kStages + s;
-        drain_bar(sm, kBarKvFull + (int)s, (last / kStages) & 1u, p);
+        if ((int64_t)last != skipped) drain_bar(sm, kBarKvFull + (int)s, (last / kStages) & 1u, p);
     }
     if (q_loads > 0) drain_bar(sm, kBarQFull, (q_loads - 1u) & 1u, p);
 }
@@ -530,6 +537,11 @@ fv_status launch_attn_fwd(const AttnLaunch &a, cudaStream_t stream) {
     p.kv_tiles = (int)((a.n + kRows - 1) / kRows);
     p.num_units = a.heads * p.q_blocks;
     p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
+    // Test hook for the failure path: FV_TEST_SKIP_KV_LOAD=<n> makes CTA 0 skip
+    // its n-th K/V tile load, so a bounded wait in the kernel runs out (about
+    // 2 s) and the call reports FV_ERR_DEVICE_TIMEOUT through fv_sync_status.
+    const char *skip = std::getenv("FV_TEST_SKIP_KV_LOAD");
+    p.skip_load = skip != nullptr ? std::atoi(skip) : -1;
     const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
     attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
