@@ -62,6 +62,12 @@ class Oracle:
         lib.oracle_gated_residual.argtypes = [u16p, u16p, ctypes.c_int64, f32p, i64p, ctypes.c_int64,
                                               f64p, u16p, ctypes.c_int]
         lib.oracle_gated_residual.restype = ctypes.c_int
+        lib.oracle_attn_rows_window.argtypes = [u16p, u16p, u16p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_double, ctypes.c_int64, ctypes.c_int64,
+                                                ctypes.c_int64, i64p, ctypes.c_int64, f64p, f64p, ctypes.c_int]
+        lib.oracle_attn_rows_window.restype = ctypes.c_int
+        lib.oracle_window_allowed.argtypes = [ctypes.c_int64] * 6
+        lib.oracle_window_allowed.restype = ctypes.c_int
         lib.oracle_round_bf16.argtypes = [ctypes.c_double]
         lib.oracle_round_bf16.restype = ctypes.c_double
         self.lib = lib
@@ -84,6 +90,28 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_attn_rows: bad arguments")
         return o, lse
+
+    def attn_rows_window(self, q, k, v, head: int, rows, scale: float, frame_tokens: int, chunk_frames: int = 5,
+                         window_chunks: int = 1, head_dim: int = 128, threads: int | None = None):
+        """fp64 windowed attention (local chunk window + first/last frame anchors)
+        of ``head`` for query ``rows``; returns (O [len(rows), head_dim], lse)."""
+        qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
+        n, ld = qb.shape
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        o = np.empty((len(rows), head_dim), dtype=np.float64)
+        lse = np.empty(len(rows), dtype=np.float64)
+        rc = self.lib.oracle_attn_rows_window(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                              _ptr(vb, ctypes.c_uint16), n, ld, head_dim, head, float(scale),
+                                              frame_tokens, chunk_frames, window_chunks, _ptr(rows, ctypes.c_int64),
+                                              len(rows), _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+                                              threads or default_threads())
+        if rc != 0:
+            raise ValueError("oracle_attn_rows_window: bad arguments")
+        return o, lse
+
+    def window_allowed(self, i: int, j: int, n: int, frame_tokens: int, chunk_frames: int = 5,
+                       window_chunks: int = 1) -> bool:
+        return bool(self.lib.oracle_window_allowed(i, j, n, frame_tokens, chunk_frames, window_chunks))
 
     def modulate(self, x, shift_row, scale_row, eps: float, rows=None, threads: int | None = None):
         """fp64 LN(x)*(1+scale_row)+shift_row for ``rows`` of x (bf16 [N, C])."""
@@ -142,6 +170,14 @@ def attn_rows(*args, **kwargs):
 
 def modulate(*args, **kwargs):
     return default().modulate(*args, **kwargs)
+
+
+def attn_rows_window(*args, **kwargs):
+    return default().attn_rows_window(*args, **kwargs)
+
+
+def window_allowed(*args, **kwargs):
+    return default().window_allowed(*args, **kwargs)
 
 
 def gated_residual(*args, **kwargs):

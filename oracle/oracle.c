@@ -24,6 +24,10 @@
  *                         a stored table).
  *   oracle_gated_residual out = x + gate[step] * a, then rounded to bfloat16
  *                         (same section: the gate of the attention branch).
+ *   oracle_attn_rows_window  the softmax branch of Video DeltaNet: the same
+ *                         attention over the keys of a local window of latent
+ *                         frames plus the first and last frame ("FreeVideo",
+ *                         section "Where Video DeltaNet comes in").
  *
  * Inputs are bfloat16 bit patterns (uint16) and float32 tables; both convert
  * exactly to double.  Work is split over rows with POSIX threads; each row is
@@ -159,6 +163,111 @@ int oracle_attn_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
         j->r_begin = nrows * w / nthreads;
         j->r_end = nrows * (w + 1) / nthreads;
         pthread_create(&tid[w], NULL, attn_worker, j);
+    }
+    for (int w = 0; w < nthreads; ++w) pthread_join(tid[w], NULL);
+    free(Kd);
+    free(Vd);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* windowed attention (Video DeltaNet softmax branch)                        */
+/* ------------------------------------------------------------------------ */
+/*
+ * Which keys query i may see ("FreeVideo", section "Where Video DeltaNet
+ * comes in"): tokens are grouped into latent frames of T tokens and frames
+ * into chunks of C frames (one VAE chunk); a query sees every key whose chunk
+ * is within W chunks of its own (W = 1: itself and its two neighbours, a
+ * 15-frame window), plus every key in the first and the last latent frame;
+ * queries in the first and the last latent frame see every key.
+ */
+int oracle_window_allowed(int64_t i, int64_t j, int64_t N, int64_t T, int64_t C, int64_t W) {
+    const int64_t frames = N / T;
+    const int64_t fi = i / T, fj = j / T;
+    if (fi == 0 || fi == frames - 1) return 1;
+    if (fj == 0 || fj == frames - 1) return 1;
+    int64_t d = fi / C - fj / C;
+    if (d < 0) d = -d;
+    return d <= W;
+}
+
+typedef struct {
+    attn_job a;
+    int64_t T, C, W;
+} win_job;
+
+static void *win_worker(void *arg) {
+    win_job *w = (win_job *)arg;
+    attn_job *j = &w->a;
+    const int64_t N = j->N;
+    const int D = j->D;
+    double *s = (double *)malloc(sizeof(double) * (size_t)N);
+    double *q = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int64_t r = j->r_begin; r < j->r_end; ++r) {
+        const int64_t i = j->rows[r];
+        for (int c = 0; c < D; ++c) q[c] = bf16_to_double(j->Q[i * j->ld + (int64_t)j->h * D + c]);
+        /* scores of the allowed keys; -inf marks a key the query may not see */
+        for (int64_t t = 0; t < N; ++t) {
+            if (!oracle_window_allowed(i, t, N, w->T, w->C, w->W)) { s[t] = -INFINITY; continue; }
+            const double *k = j->Kd + t * D;
+            double dot = 0.0;
+            for (int c = 0; c < D; ++c) dot += q[c] * k[c];
+            s[t] = j->scale * dot;
+        }
+        double m = -INFINITY;
+        for (int64_t t = 0; t < N; ++t) if (s[t] > m) m = s[t];
+        double l = 0.0;
+        for (int64_t t = 0; t < N; ++t) { s[t] = (s[t] == -INFINITY) ? 0.0 : exp(s[t] - m); l += s[t]; }
+        double *o = j->O + r * D;
+        for (int c = 0; c < D; ++c) o[c] = 0.0;
+        for (int64_t t = 0; t < N; ++t) {
+            if (s[t] == 0.0) continue;
+            const double *v = j->Vd + t * D;
+            for (int c = 0; c < D; ++c) o[c] += s[t] * v[c];
+        }
+        for (int c = 0; c < D; ++c) o[c] /= l;
+        j->lse[r] = m + log(l);
+    }
+    free(q);
+    free(s);
+    return NULL;
+}
+
+/*
+ * Windowed attention of head h for query rows rows[0..nrows): the same as
+ * oracle_attn_rows over the keys oracle_window_allowed admits.  N must be a
+ * multiple of T.
+ */
+int oracle_attn_rows_window(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                            int64_t N, int64_t ld, int D, int h, double scale,
+                            int64_t T, int64_t C, int64_t W,
+                            const int64_t *rows, int64_t nrows,
+                            double *O, double *lse, int nthreads) {
+    if (!Q || !K || !V || !rows || !O || !lse || N < 1 || D < 1 || h < 0 ||
+        ld < (int64_t)(h + 1) * D || nrows < 0 || T < 1 || N % T != 0 || C < 1 || W < 0)
+        return -1;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= N) return -1;
+    if (nrows == 0) return 0;
+    double *Kd = (double *)malloc(sizeof(double) * (size_t)N * (size_t)D);
+    double *Vd = (double *)malloc(sizeof(double) * (size_t)N * (size_t)D);
+    if (!Kd || !Vd) { free(Kd); free(Vd); return -1; }
+    for (int64_t t = 0; t < N; ++t)
+        for (int c = 0; c < D; ++c) {
+            Kd[t * D + c] = bf16_to_double(K[t * ld + (int64_t)h * D + c]);
+            Vd[t * D + c] = bf16_to_double(V[t * ld + (int64_t)h * D + c]);
+        }
+    nthreads = clamp_threads(nthreads, nrows);
+    pthread_t tid[256];
+    win_job job[256];
+    for (int w = 0; w < nthreads; ++w) {
+        attn_job *j = &job[w].a;
+        j->Q = Q; j->Kd = Kd; j->Vd = Vd; j->N = N; j->ld = ld; j->D = D; j->h = h;
+        j->scale = scale; j->rows = rows; j->O = O; j->lse = lse;
+        j->r_begin = nrows * w / nthreads;
+        j->r_end = nrows * (w + 1) / nthreads;
+        job[w].T = T; job[w].C = C; job[w].W = W;
+        pthread_create(&tid[w], NULL, win_worker, &job[w]);
     }
     for (int w = 0; w < nthreads; ++w) pthread_join(tid[w], NULL);
     free(Kd);

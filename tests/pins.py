@@ -311,3 +311,67 @@ def round_bf16_cases(orc) -> None:
     assert r(3.39e38) == 255.0 * 2.0 ** 120                             # largest finite bf16
     assert math.isinf(r(3.40e38))                                       # past the last half step
     assert r(0.0) == 0.0 and math.isnan(r(float("nan")))
+
+
+# ------------------------------------------------------- windowed attention
+def window_mask_numpy(n: int, t: int, c: int, w: int) -> np.ndarray:
+    """The window written out independently of the oracle: frames of t tokens,
+    chunks of c frames, chunk distance <= w, plus first/last frame anchors."""
+    frames = n // t
+    f = np.arange(n) // t
+    ch = f // c
+    allowed = np.abs(ch[:, None] - ch[None, :]) <= w
+    anchor = (f == 0) | (f == frames - 1)
+    return allowed | anchor[:, None] | anchor[None, :]
+
+
+def window_brute_force(orc, n: int, t: int, c: int, w: int, seed: int) -> float:
+    q = _rand_bf16((n, 2 * D), seed)
+    k = _rand_bf16((n, 2 * D), seed + 1)
+    v = _rand_bf16((n, 2 * D), seed + 2)
+    scale = 1.0 / math.sqrt(D)
+    mask = window_mask_numpy(n, t, c, w)
+    worst = 0.0
+    for h in range(2):
+        s = scale * (_head(q, h) @ _head(k, h).T)
+        s = np.where(mask, s, -np.inf)
+        o_ref = scipy.special.softmax(s, axis=1) @ _head(v, h)
+        lse_ref = scipy.special.logsumexp(s, axis=1)
+        o, lse = orc.attn_rows_window(q, k, v, h, np.arange(n), scale, t, c, w)
+        worst = max(worst, _rel(o, o_ref), _rel(lse, lse_ref))
+    return worst
+
+
+def window_structure(orc) -> None:
+    n, t, c, w = 12 * 16, 16, 3, 1        # 12 frames of 16 tokens, chunks of 3 frames
+    scale = 1.0 / math.sqrt(D)
+    q = _rand_bf16((n, D), 71)
+    k = _rand_bf16((n, D), 72)
+    v = _rand_bf16((n, D), 73)
+    rows = np.arange(n)
+    o_win, l_win = orc.attn_rows_window(q, k, v, 0, rows, scale, t, c, w)
+    o_den, l_den = orc.attn_rows(q, k, v, 0, rows, scale)
+    # a window wider than the clip is dense attention
+    o_all, l_all = orc.attn_rows_window(q, k, v, 0, rows, scale, t, c, 12)
+    assert _rel(o_all, o_den) < 1e-13 and _rel(l_all, l_den) < 1e-13
+    # queries in the first and last frame see every key
+    anchor_rows = np.r_[0:t, n - t:n]
+    assert np.array_equal(o_win[anchor_rows], o_den[anchor_rows])
+    # a middle query differs from dense attention, and ignores keys outside its window
+    i = 6 * t + 5                          # frame 6, chunk 2: sees chunks 1-3 (frames 3-11) and frame 0
+    assert np.max(np.abs(o_win[i] - o_den[i])) > 1e-6
+    hidden = np.r_[t:3 * t]                # frames 1-2 (chunk 0 minus the anchor frame 0)
+    k2, v2 = k.clone(), v.clone()
+    k2[hidden] = 7.0
+    v2[hidden] = -3.0
+    o2, _ = orc.attn_rows_window(q, k2, v2, 0, [i], scale, t, c, w)
+    assert np.array_equal(o2[0], o_win[i])
+    seen = np.r_[4 * t:4 * t + 3]           # frame 4 is inside the window
+    k3 = k.clone()
+    k3[seen] = 2.0
+    o3, _ = orc.attn_rows_window(q, k3, v, 0, [i], scale, t, c, w)
+    assert np.max(np.abs(o3[0] - o_win[i])) > 1e-6
+    # the window is symmetric and matches the independent numpy statement
+    m = window_mask_numpy(n, t, c, w)
+    got = np.array([[orc.window_allowed(a, b, n, t, c, w) for b in range(0, n, 4)] for a in range(0, n, 4)])
+    assert np.array_equal(got, m[::4, ::4]) and np.array_equal(m, m.T)

@@ -82,3 +82,22 @@ def test_round_bf16_matches_torch_on_float32_values():
     ref = f.to(torch.bfloat16).to(torch.float64).numpy()
     got = np.array([oracle.round_bf16(float(v)) for v in f.tolist()])
     assert np.array_equal(ref, got)
+
+
+# ------------------------------------------------------- windowed attention
+@pytest.mark.parametrize("n,t,c,w", [(10 * 8, 8, 2, 1), (7 * 30, 30, 3, 1), (5 * 13, 13, 5, 1), (9 * 4, 4, 1, 2)])
+def test_window_brute_force(n, t, c, w):
+    assert pins.window_brute_force(oracle, n, t, c, w, seed=n) < 1e-12
+
+
+def test_window_structure():
+    pins.window_structure(oracle)
+
+
+def test_window_density_under_this_reading():
+    """Video-only share of admitted (query, key) frame pairs at 42 and 102
+    latent frames; the pages quote 42.1 % and 20.0 % for sequences that also
+    hold text and audio tokens, which see and are seen by everything."""
+    for frames, expect in ((42, 0.400), (102, 0.177)):
+        got = sum(oracle.window_allowed(a, b, frames, 1) for a in range(frames) for b in range(frames)) / frames ** 2
+        assert abs(got - expect) < 5e-4

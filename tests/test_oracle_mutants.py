@@ -27,6 +27,10 @@ MUTANTS = {
                       "bf16_to_double(x[c]) - (double)j->t0[c] * bf16_to_double(a[c])"),
     "round_via_float": ("double r = nearbyint(ldexp(x, -q));", "double r = nearbyint(ldexp((double)(float)x, -q));"),
     "round_truncates": ("double r = nearbyint(ldexp(x, -q));", "double r = trunc(ldexp(x, -q));"),
+    "window_no_anchor_rows": ("if (fi == 0 || fi == frames - 1) return 1;", ""),
+    "window_no_anchor_keys": ("if (fj == 0 || fj == frames - 1) return 1;", ""),
+    "window_off_by_one": ("return d <= W;", "return d < W;"),
+    "window_chunks_of_tokens": ("int64_t d = fi / C - fj / C;", "int64_t d = i / C - j / C;"),
 }
 
 
@@ -44,6 +48,8 @@ def _all_pins(orc):
         "modulate_closed": lambda: pins.modulate_closed_forms(orc) is None,
         "residual_closed": lambda: pins.gated_residual_closed_forms(orc) is None,
         "rounding": lambda: pins.round_bf16_cases(orc) is None,
+        "window_brute": lambda: pins.window_brute_force(orc, 7 * 30, 30, 3, 1, seed=5) < 1e-12,
+        "window_structure": lambda: pins.window_structure(orc) is None,
     }
     failed = []
     for name, fn in checks.items():
@@ -64,9 +70,9 @@ def test_unmutated_oracle_passes_every_pin():
 def test_mutant_is_caught(name, tmp_path):
     src = open(obuild.SRC).read()
     old, new = MUTANTS[name]
-    assert src.count(old) == 1, f"mutation anchor for {name} not found once"
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
     mutated = tmp_path / "oracle_mutant.c"
-    mutated.write_text(src.replace(old, new))
+    mutated.write_text(src.replace(old, new))  # every occurrence (dense and windowed paths)
     lib = tmp_path / "liboracle_mutant.so"
     subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", str(mutated), "-o", str(lib), "-lm"],
                    check=True)
