@@ -92,6 +92,34 @@ fv_status fv_attn_fwd(const void *Q, const void *K, const void *V, void *O,
                       float *lse, void *stream);
 
 /*
+ * Windowed softmax attention: the softmax branch of Video DeltaNet
+ * ("FreeVideo: a 66 GB video transformer on an 8 GB card", section "Where
+ * Video DeltaNet comes in"): softmax attention stays exact but only within a
+ * window; each query chunk of five latent frames (one VAE chunk) sees itself
+ * and its two neighbours, every frame sees the first and the last latent
+ * frame, and those two frames see everything.
+ *
+ * Tokens form latent frames of frame_tokens tokens (N must be a multiple of
+ * frame_tokens; frames = N / frame_tokens); frames form chunks of
+ * chunk_frames frames counted from frame 0 (the last chunk may be short).
+ * Query i in frame f (chunk c = f / chunk_frames) sees key j in frame g when
+ *   f is the first or the last frame, or g is the first or the last frame,
+ *   or |g / chunk_frames - c| <= window_chunks,
+ * and O is softmax attention over exactly those keys (same arithmetic and
+ * output conventions as fv_attn_fwd; lse is over the admitted keys).
+ * The kernel visits only the K/V tiles some row of a 256-row block may see.
+ *
+ * frame_tokens >= 1 with N % frame_tokens == 0; chunk_frames >= 1;
+ * window_chunks >= 0; otherwise FV_ERR_SHAPE.  The model's values are
+ * frame_tokens = (H/32)(W/32) (1,008 at 1344x768), chunk_frames = 5,
+ * window_chunks = 1.  All other arguments as fv_attn_fwd.
+ */
+fv_status fv_attn_fwd_window(const void *Q, const void *K, const void *V, void *O,
+                             int64_t N, int H, int D, float scale, int head_group,
+                             int frame_tokens, int chunk_frames, int window_chunks,
+                             float *lse, void *stream);
+
+/*
  * Cached-AdaLN modulated LayerNorm of the residual stream for one schedule step:
  *   mu = mean_c x[i,c],  var = mean_c (x[i,c] - mu)^2   (biased)
  *   y[i,c] = (x[i,c] - mu) / sqrt(var + eps) * (1 + scale_table[step*ld + c])

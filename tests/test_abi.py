@@ -124,3 +124,20 @@ def test_product_package_never_imports_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cc", ".cpp")):
                 text = open(os.path.join(root, f)).read()
                 assert "oracle" not in text.lower(), f
+
+
+def window(lib, n=4032, t=1008, c=5, w=1, **kw):
+    return lib.fv_attn_fwd_window(A, B, C, O, n, 4, 128, 0.088, 4, t, c, w, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(t=0), -2), (dict(t=1000), -2), (dict(c=0), -2), (dict(w=-1), -2), (dict(n=0), -2),
+])
+def test_window_rejects_bad_arguments(lib, kw, code):
+    assert window(lib, **kw) == code
+
+
+def test_window_null_pointers(lib):
+    assert lib.fv_attn_fwd_window(None, B, C, O, 4032, 4, 128, 0.088, 4, 1008, 5, 1, None, None) == -1
+    assert lib.fv_attn_fwd_window(A, B, C, O, 4032, 4, 128, 0.088, 4, 1008, 5, 1, T + 2, None) == -3
+    assert lib.fv_attn_fwd_window(A, B, C, O, 4032, 4, 128, 0.088, 4, 1008, 5, 1, A + 4, None) == -9

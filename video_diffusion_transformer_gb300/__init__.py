@@ -24,7 +24,7 @@ STATUS = {
 }
 # every symbol include/fv.h declares
 EXPORTS = ("fv_attn_fwd", "fv_adaln_modulate", "fv_gated_residual", "fv_step_for_timestep", "fv_sync_status",
-           "fv_status_string", "fv_version", "fv_attn_fwd_noalloc")
+           "fv_status_string", "fv_version", "fv_attn_fwd_noalloc", "fv_attn_fwd_window")
 NOALLOC_MAX_LAUNCHES = 64
 
 HEAD_DIM = 128
@@ -53,6 +53,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
     lib.fv_attn_fwd.argtypes = [vp, vp, vp, vp, i64, i32, i32, f32, i32, vp, vp]
     lib.fv_attn_fwd.restype = i32
+    lib.fv_attn_fwd_window.argtypes = [vp, vp, vp, vp, i64, i32, i32, f32, i32, i32, i32, i32, vp, vp]
+    lib.fv_attn_fwd_window.restype = i32
     lib.fv_adaln_modulate.argtypes = [vp, vp, i32, i64, i32, vp, vp, i64, i32, i32, f32, vp]
     lib.fv_adaln_modulate.restype = i32
     lib.fv_gated_residual.argtypes = [vp, vp, vp, i64, i32, vp, i64, i32, i32, vp]
@@ -123,6 +125,33 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tenso
     code = load_library().fv_attn_fwd(*ptrs, n, h, HEAD_DIM, float(scale), int(min(head_group, h)), lse_ptr,
                                       _stream_ptr(stream))
     _check(code, "fv_attn_fwd")
+    return out
+
+
+def attn_fwd_window(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor | None = None, *,
+                    frame_tokens: int, chunk_frames: int = 5, window_chunks: int = 1, heads: int | None = None,
+                    head_group: int = 16, scale: float = DEFAULT_SCALE, lse: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """Windowed softmax attention (the Video DeltaNet softmax branch): queries see
+    keys in latent-frame chunks within ``window_chunks`` of their own, plus the
+    first and last frame; queries in those two frames see every key."""
+    n = q.shape[0]
+    width = q.numel() // max(1, n)
+    h = heads if heads is not None else width // HEAD_DIM
+    if h * HEAD_DIM != width or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [N, H*128]")
+    if out is None:
+        out = torch.empty_like(q)
+    ptrs = [_dev(t, nm, torch.bfloat16) for t, nm in ((q, "q"), (k, "k"), (v, "v"), (out, "out"))]
+    lse_ptr = None
+    if lse is not None:
+        if lse.shape != (h, n):
+            raise ValueError("lse must be float32 [H, N]")
+        lse_ptr = _dev(lse, "lse", torch.float32)
+    code = load_library().fv_attn_fwd_window(*ptrs, n, h, HEAD_DIM, float(scale), int(min(head_group, h)),
+                                             int(frame_tokens), int(chunk_frames), int(window_chunks), lse_ptr,
+                                             _stream_ptr(stream))
+    _check(code, "fv_attn_fwd_window")
     return out
 
 

@@ -94,7 +94,80 @@ struct Params {
     int num_units;   // heads * q_blocks
     float scale_log2;  // scale * log2(e)
     int skip_load;     // test hook: CTA 0 never issues its K/V load number skip_load (-1: off)
+    // windowed attention (0 frame tokens: dense): tokens form latent frames of
+    // frame_tokens, frames form chunks of chunk_frames; a query sees the keys
+    // of chunks within window_chunks of its own, plus the first and the last
+    // frame; queries in the first and the last frame see every key.
+    int frame_tokens, chunk_frames, window_chunks;
 };
+
+// The K/V tiles one work unit visits: up to three ascending, disjoint ranges
+// of tile indices.  Every role derives the same list from the unit.
+struct KvList {
+    int lo[3], hi[3];
+    int count;
+    __device__ __forceinline__ int tile(int idx) const {
+        const int n0 = hi[0] - lo[0];
+        if (idx < n0) return lo[0] + idx;
+        idx -= n0;
+        const int n1 = hi[1] - lo[1];
+        if (idx < n1) return lo[1] + idx;
+        return lo[2] + (idx - n1);
+    }
+};
+
+__device__ __forceinline__ int frames_of(const Params &p) { return p.n / p.frame_tokens; }
+
+// Window of the keys one query row sees, in tokens: [w0, w1) plus the anchor
+// frames; anchor = the row sees every key.
+struct RowWindow {
+    int w0, w1;
+    bool anchor;
+};
+
+__device__ __forceinline__ RowWindow row_window(const Params &p, int row) {
+    RowWindow r;
+    const int T = p.frame_tokens, C = p.chunk_frames, frames = frames_of(p);
+    const int f = row / T;
+    r.anchor = f == 0 || f >= frames - 1;  // rows past the end are never stored
+    const int c = f / C;
+    r.w0 = max(0, (c - p.window_chunks) * C) * T;
+    r.w1 = min(frames, (c + p.window_chunks + 1) * C) * T;
+    return r;
+}
+
+template <bool kWindow>
+__device__ __forceinline__ KvList kv_list(const Params &p, int qb) {
+    KvList L;
+    L.lo[0] = 0;
+    L.hi[0] = p.kv_tiles;
+    L.lo[1] = L.hi[1] = L.lo[2] = L.hi[2] = 0;
+    L.count = p.kv_tiles;
+    if (!kWindow) return L;
+    const int T = p.frame_tokens, C = p.chunk_frames, frames = frames_of(p);
+    const int r0 = qb * kUnitRows;
+    const int r1 = min(p.n, r0 + kUnitRows);
+    const int f0 = r0 / T, f1 = (r1 - 1) / T;
+    if (f0 == 0 || f1 >= frames - 1) return L;  // an anchor row: every key
+    // key tokens: first frame, the union of the rows' windows, last frame
+    const int x[3][2] = {{0, T},
+                         {max(0, (f0 / C - p.window_chunks) * C) * T, min(frames, (f1 / C + p.window_chunks + 1) * C) * T},
+                         {(frames - 1) * T, p.n}};
+    int m = 0;
+    for (int r = 0; r < 3; ++r) {
+        const int lo = x[r][0] / kRows, hi = (x[r][1] + kRows - 1) / kRows;
+        if (m > 0 && lo <= L.hi[m - 1]) {
+            L.hi[m - 1] = max(L.hi[m - 1], hi);
+        } else {
+            L.lo[m] = lo;
+            L.hi[m] = hi;
+            ++m;
+        }
+    }
+    for (int r = m; r < 3; ++r) L.lo[r] = L.hi[r] = 0;
+    L.count = (L.hi[0] - L.lo[0]) + (L.hi[1] - L.lo[1]) + (L.hi[2] - L.lo[2]);
+    return L;
+}
 
 struct Smem {
     uint32_t q, kv, bar;
@@ -113,6 +186,7 @@ __device__ __forceinline__ void drain_bar(const Smem &sm, int i, uint32_t parity
 }
 
 // ------------------------------------------------------------------ TMA
+template <bool kWindow>
 __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv, const Params &p,
                          const Smem &sm) {
     uint32_t loads = 0;     // K/V tiles issued into the ring
@@ -135,7 +209,9 @@ __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUt
             ptx::tma_load_2d(dst + kHalfBytes, tq, sm.b(kBarQFull), x0 + 64, y);
         }
         ++q_loads;
-        for (int j = 0; ok && j < p.kv_tiles; ++j) {
+        const KvList kl = kv_list<kWindow>(p, qb);
+        for (int j = 0; ok && j < kl.count; ++j) {
+            const int kv_row = kl.tile(j) * kRows;
             for (int w = 0; w < 2; ++w) {
                 const uint32_t s = loads % kStages, ph = (loads / kStages) & 1u;
                 ok = wait_bar(sm, kBarKvEmpty + (int)s, ph ^ 1u, p, kWhereKvEmpty);
@@ -144,8 +220,8 @@ __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUt
                     ptx::mbar_arrive_expect_tx(sm.b(kBarKvFull + (int)s), kTileBytes);
                     const CUtensorMap *m = w ? tv : tk;
                     const uint32_t dst = sm.kv + s * (uint32_t)kTileBytes;
-                    ptx::tma_load_2d(dst, m, sm.b(kBarKvFull + (int)s), x0, j * kRows);
-                    ptx::tma_load_2d(dst + kHalfBytes, m, sm.b(kBarKvFull + (int)s), x0 + 64, j * kRows);
+                    ptx::tma_load_2d(dst, m, sm.b(kBarKvFull + (int)s), x0, kv_row);
+                    ptx::tma_load_2d(dst + kHalfBytes, m, sm.b(kBarKvFull + (int)s), x0 + 64, kv_row);
                 }
                 ++loads;
             }
@@ -194,6 +270,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
     }
 }
 
+template <bool kWindow>
 __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
     MmaDescs dsc;
     dsc.q0 = ptx::sdesc_sw128(sm.q, 16, 1024);
@@ -206,6 +283,7 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
     for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
         ok = wait_bar(sm, kBarQFull, units & 1u, p, kWhereQFull);
         if (!ok) break;
+        const int n_kv = kv_list<kWindow>(p, unit % p.q_blocks).count;
         {
             const uint32_t s = ring % kStages;
             ok = wait_bar(sm, kBarKvFull + (int)s, (ring / kStages) & 1u, p, kWhereKvFull);
@@ -219,10 +297,10 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
             }
             ptx::tc_commit(sm.b(kBarKvEmpty + (int)s));
         }
-        for (int j = 0; ok && j < p.kv_tiles; ++j) {
+        for (int j = 0; ok && j < n_kv; ++j) {
             const uint32_t iv = ring + 2u * (uint32_t)j + 1u, sv = iv % kStages;
             const uint32_t ik = iv + 1u, sk = ik % kStages;
-            const bool more = j + 1 < p.kv_tiles;
+            const bool more = j + 1 < n_kv;
             ok = wait_bar(sm, kBarKvFull + (int)sv, (iv / kStages) & 1u, p, kWhereKvFull);
             if (!ok) break;
             const uint64_t vdesc = dsc.v0 + sv * kDescTile;
@@ -250,7 +328,7 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
         }
         if (!ok) break;
         ptx::tc_commit(sm.b(kBarQEmpty));
-        ring += 2u * (uint32_t)p.kv_tiles;
+        ring += 2u * (uint32_t)n_kv;
         ++units;
     }
     // Every MMA issued must complete before the tensor memory is released.
@@ -267,9 +345,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Row maximum of the 128 raw scores; columns >= valid are ignored.
-template <bool kMasked>
-__device__ __forceinline__ float row_max(const uint32_t (&s)[4][32], int valid) {
+// Which of a tile's 128 key columns one row may see.  Column c is admitted
+// when c < valid (inside the sequence) and either the row sees every key, or
+// c falls in the first frame (c < a0), in the row's window (w0 <= c < w1) or
+// in the last frame (c >= a1).  All bounds are relative to the tile's first key.
+// Dense attention only ever masks the ragged end of the sequence.
+template <bool kWindow>
+struct ColMask {
+    int valid, a0, w0, w1, a1;
+    bool all;
+    __device__ __forceinline__ bool ok(int c) const {
+        if (!kWindow) return c < valid;
+        return c < valid && (all || c < a0 || (c >= w0 && c < w1) || c >= a1);
+    }
+};
+
+// Row maximum of the 128 raw scores; columns the mask rejects are ignored.
+template <bool kMasked, bool kWindow>
+__device__ __forceinline__ float row_max(const uint32_t (&s)[4][32], const ColMask<kWindow> &cm) {
     if (!kMasked) {
         // two independent chains of three-input maxima
         float m0 = -INFINITY, m1 = -INFINITY;
@@ -287,16 +380,16 @@ __device__ __forceinline__ float row_max(const uint32_t (&s)[4][32], int valid) 
     for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-            if (c4 * 32 + i < valid) m = fmaxf(m, u2f(s[c4][i]));
+            if (cm.ok(c4 * 32 + i)) m = fmaxf(m, u2f(s[c4][i]));
     return m;
 }
 
 // p = 2^(s * scale_log2 - m) rounded to bf16 pairs and stored over the first
 // 64 columns of S; returns the float32 sum of p.  Pairs of columns share one
 // packed multiply-add and one packed add.
-template <bool kMasked>
-__device__ __forceinline__ float write_probs(const uint32_t (&s)[4][32], int valid, float scale_log2, float m,
-                                             uint32_t t_s) {
+template <bool kMasked, bool kWindow>
+__device__ __forceinline__ float write_probs(const uint32_t (&s)[4][32], const ColMask<kWindow> &cm,
+                                             float scale_log2, float m, uint32_t t_s) {
     float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4) {
@@ -311,10 +404,10 @@ __device__ __forceinline__ float write_probs(const uint32_t (&s)[4][32], int val
             float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
             float p2 = ptx::ex2_approx(x2), p3 = ptx::ex2_approx(x3);
             if (kMasked) {
-                p0 = c < valid ? p0 : 0.f;
-                p1 = c + 1 < valid ? p1 : 0.f;
-                p2 = c + 2 < valid ? p2 : 0.f;
-                p3 = c + 3 < valid ? p3 : 0.f;
+                p0 = cm.ok(c) ? p0 : 0.f;
+                p1 = cm.ok(c + 1) ? p1 : 0.f;
+                p2 = cm.ok(c + 2) ? p2 : 0.f;
+                p3 = cm.ok(c + 3) ? p3 : 0.f;
             }
             ptx::add2(a0, a1, p0, p1);
             ptx::add2(b0, b1, p2, p3);
@@ -326,6 +419,7 @@ __device__ __forceinline__ float write_probs(const uint32_t (&s)[4][32], int val
     return (a0 + a1) + (b0 + b1);
 }
 
+template <bool kWindow>
 __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int k, int t) {
     const uint32_t lane_base = (uint32_t)((t >> 5) * 32) << 16;
     const uint32_t t_s = tmem + lane_base + (uint32_t)(128 * k);
@@ -335,8 +429,17 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
     for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
         const int head = p.head_begin + unit / p.q_blocks;
         const int row = (unit % p.q_blocks) * kUnitRows + k * kRows + t;
+        const KvList kl = kv_list<kWindow>(p, unit % p.q_blocks);
+        const int n_kv = kWindow ? kl.count : p.kv_tiles;
+        RowWindow rw = {0, 0, true};
+        int first_end = 0, last_begin = 0;
+        if (kWindow) {
+            rw = row_window(p, row);
+            first_end = p.frame_tokens;
+            last_begin = (frames_of(p) - 1) * p.frame_tokens;
+        }
         float m_used = -INFINITY, l = 0.f;
-        for (int j = 0; j < p.kv_tiles; ++j) {
+        for (int j = 0; j < n_kv; ++j) {
             ok = __all_sync(0xffffffffu, wait_bar(sm, kBarSFull + k, tile & 1u, p, kWhereSFull));
             if (!ok) break;
             ptx::tc_fence_after();
@@ -346,9 +449,21 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) ptx::reg_fence(s[c4]);
-            const int valid = p.n - j * kRows;
-            const bool masked = valid < kRows;
-            const float m_tile = (masked ? row_max<true>(s, valid) : row_max<false>(s, valid)) * p.scale_log2;
+            const int kb = (kWindow ? kl.tile(j) : j) * kRows;
+            ColMask<kWindow> cm;
+            cm.valid = p.n - kb;
+            cm.all = !kWindow || rw.anchor;
+            cm.a0 = first_end - kb;
+            cm.w0 = rw.w0 - kb;
+            cm.w1 = rw.w1 - kb;
+            cm.a1 = last_begin - kb;
+            bool need = cm.valid < kRows;
+            if (kWindow && !cm.all)
+                need = need || !((cm.w0 <= 0 && cm.w1 >= kRows) || cm.a0 >= kRows || cm.a1 <= 0);
+            // one code path per warp: the tcgen05 copies are warp-collective
+            const bool masked = __any_sync(0xffffffffu, need);
+            const float m_tile =
+                (masked ? row_max<true, kWindow>(s, cm) : row_max<false, kWindow>(s, cm)) * p.scale_log2;
             float factor = 1.f;
             bool rescale = false;
             if (j == 0) {
@@ -358,8 +473,8 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
                 m_used = m_tile;
                 rescale = true;
             }
-            const float tile_sum = masked ? write_probs<true>(s, valid, p.scale_log2, m_used, t_s)
-                                          : write_probs<false>(s, valid, p.scale_log2, m_used, t_s);
+            const float tile_sum = masked ? write_probs<true, kWindow>(s, cm, p.scale_log2, m_used, t_s)
+                                          : write_probs<false, kWindow>(s, cm, p.scale_log2, m_used, t_s);
             l = l * factor + tile_sum;
             // O (complete through tile j-1, since S_j is) must carry the new maximum
             // before the next P.V accumulates into it.
@@ -411,6 +526,7 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
     }
 }
 
+template <bool kWindow>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -457,11 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
 
     if (warp == kTmaWarp) {
-        if (lane == 0) producer(&tm_q, &tm_k, &tm_v, p, sm);
+        if (lane == 0) producer<kWindow>(&tm_q, &tm_k, &tm_v, p, sm);
     } else if (warp == kMmaWarp) {
-        if (lane == 0) mma_issuer(p, sm, tmem);
+        if (lane == 0) mma_issuer<kWindow>(p, sm, tmem);
     } else {
-        softmax_role(p, sm, tmem, warp >> 2, (int)threadIdx.x & 127);
+        softmax_role<kWindow>(p, sm, tmem, warp >> 2, (int)threadIdx.x & 127);
     }
     __syncwarp();  // lanes 1-31 of the TMA and MMA warps wait here for lane 0
     ptx::tc_fence_before();
@@ -510,16 +626,18 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t n, int ld) {
 
 fv_status launch_attn_fwd(const AttnLaunch &a, cudaStream_t stream) {
     static std::mutex mu;
-    static bool attr_set[64] = {};
+    static bool attr_set[64][2] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FV_ERR_LAUNCH;
     {
         std::lock_guard<std::mutex> g(mu);
-        if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-                cudaSuccess)
+        if (!attr_set[dev][0]) {
+            if (cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemBytes) != cudaSuccess ||
+                cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemBytes) != cudaSuccess)
                 return FV_ERR_LAUNCH;
-            attr_set[dev] = true;
+            attr_set[dev][0] = attr_set[dev][1] = true;
         }
     }
     const int ld = a.heads_total * kD;
@@ -542,8 +660,14 @@ fv_status launch_attn_fwd(const AttnLaunch &a, cudaStream_t stream) {
     // 2 s) and the call reports FV_ERR_DEVICE_TIMEOUT through fv_sync_status.
     const char *skip = std::getenv("FV_TEST_SKIP_KV_LOAD");
     p.skip_load = skip != nullptr ? std::atoi(skip) : -1;
+    p.frame_tokens = a.frame_tokens;
+    p.chunk_frames = a.chunk_frames;
+    p.window_chunks = a.window_chunks;
     const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
-    attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    if (a.frame_tokens > 0)
+        attn_fwd_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    else
+        attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
 }
 

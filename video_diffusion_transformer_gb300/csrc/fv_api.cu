@@ -61,12 +61,11 @@ fv_status device_state(DeviceState **out) {
     return FV_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-fv_status fv_attn_fwd(const void *Q, const void *K, const void *V, void *O, int64_t N, int H, int D, float scale,
-                      int head_group, float *lse, void *stream) {
+// Shared by the dense and the windowed entry points: host checks, then one
+// launch per head group.
+fv_status attn_common(const void *Q, const void *K, const void *V, void *O, int64_t N, int H, int D, float scale,
+                      int head_group, int frame_tokens, int chunk_frames, int window_chunks, float *lse,
+                      void *stream) {
     if (!Q || !K || !V || !O) return FV_ERR_NULL;
     if (D != 128 || N < 1 || N >= (int64_t(1) << 31) || H < 1 || H > 256 || head_group < 1 || head_group > H)
         return FV_ERR_SHAPE;
@@ -96,6 +95,9 @@ fv_status fv_attn_fwd(const void *Q, const void *K, const void *V, void *O, int6
     a.scale = scale;
     a.status = d->status;
     a.num_sms = d->num_sms;
+    a.frame_tokens = frame_tokens;
+    a.chunk_frames = chunk_frames;
+    a.window_chunks = window_chunks;
     for (int h0 = 0; h0 < H; h0 += head_group) {
         a.head_begin = h0;
         a.heads = (H - h0) < head_group ? (H - h0) : head_group;
@@ -103,6 +105,26 @@ fv_status fv_attn_fwd(const void *Q, const void *K, const void *V, void *O, int6
         if (st != FV_OK) return st;
     }
     return FV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fv_status fv_attn_fwd(const void *Q, const void *K, const void *V, void *O, int64_t N, int H, int D, float scale,
+                      int head_group, float *lse, void *stream) {
+    return attn_common(Q, K, V, O, N, H, D, scale, head_group, 0, 0, 0, lse, stream);
+}
+
+fv_status fv_attn_fwd_window(const void *Q, const void *K, const void *V, void *O, int64_t N, int H, int D,
+                             float scale, int head_group, int frame_tokens, int chunk_frames, int window_chunks,
+                             float *lse, void *stream) {
+    if (frame_tokens < 1 || chunk_frames < 1 || window_chunks < 0 || N < 1 || (N % frame_tokens) != 0) {
+        if (!Q || !K || !V || !O) return FV_ERR_NULL;
+        return FV_ERR_SHAPE;
+    }
+    return attn_common(Q, K, V, O, N, H, D, scale, head_group, frame_tokens, chunk_frames, window_chunks, lse,
+                       stream);
 }
 
 fv_status fv_adaln_modulate(const void *x, void *y, int y_is_fp32, int64_t N, int C, const float *shift_table,

@@ -23,6 +23,8 @@ struct AttnLaunch {
     float scale;
     int *status;       // device status word
     int num_sms;
+    // windowed attention; frame_tokens == 0 selects dense attention
+    int frame_tokens = 0, chunk_frames = 0, window_chunks = 0;
 };
 
 // Enqueue one head-group launch of the attention kernel.

@@ -80,6 +80,23 @@ def attention_flops(n: int, heads: int = NUM_HEADS, d: int = HEAD_DIM) -> float:
     return 4.0 * float(n) * float(n) * d * heads
 
 
+def window_pairs(n: int, frame_tokens: int, chunk_frames: int = 5, window_chunks: int = 1) -> int:
+    """(query, key) pairs the Video DeltaNet softmax window admits, for FLOP
+    accounting: counted over latent-frame pairs, times frame_tokens^2."""
+    frames = n // frame_tokens
+    pairs = 0
+    for f in range(frames):
+        if f in (0, frames - 1):
+            pairs += frames
+            continue
+        c = f // chunk_frames
+        lo = max(0, (c - window_chunks) * chunk_frames)
+        hi = min(frames, (c + window_chunks + 1) * chunk_frames)
+        seen = set(range(lo, hi)) | {0, frames - 1}
+        pairs += len(seen)
+    return pairs * frame_tokens * frame_tokens
+
+
 # --------------------------------------------------------------------------
 # workload table
 # --------------------------------------------------------------------------
