@@ -283,6 +283,31 @@ def run_fv(args):
         ms_total = start.elapsed_time(end)
         attn_ms = [e0.elapsed_time(e1) for e0, e1 in ev_a]
 
+        # ---- windowed attention (the Video DeltaNet softmax branch) on the same Q, K, V
+        window = None
+        if not args.no_window and w.n % W.tokens_per_latent_frame(1344, 768) == 0:
+            t_f = W.tokens_per_latent_frame(1344, 768)
+            ow = torch.empty_like(q)
+            for _ in range(2):
+                fv.attn_fwd_window(q, k, v, ow, frame_tokens=t_f, chunk_frames=5, window_chunks=1,
+                                   head_group=w.head_group, stream=stream)
+            reps = 5
+            w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            w0.record(stream)
+            for _ in range(reps):
+                fv.attn_fwd_window(q, k, v, ow, frame_tokens=t_f, chunk_frames=5, window_chunks=1,
+                                   head_group=w.head_group, stream=stream)
+            w1.record(stream)
+            torch.cuda.synchronize(dev)
+            fv.sync_status(stream)
+            wms = w0.elapsed_time(w1) / reps
+            pairs = W.window_pairs(w.n, t_f, 5, 1)
+            window = {"kernel": "attn_fwd_kernel (window)", "frame_tokens": t_f, "chunk_frames": 5,
+                      "window_chunks": 1, "density": pairs / float(w.n) ** 2, "ms": wms,
+                      "effective_tflops": 4.0 * W.HEAD_DIM * w.heads * pairs / (wms / 1e3) / 1e12,
+                      "speedup_vs_dense": (sum(attn_ms) / len(attn_ms)) / wms}
+
         # ---- end to end through the C ABI: pinned host inputs in, results out.
         # Every step copies its own inputs host->device and reads its results
         # back; copies run on their own streams, double-buffered, so step i's
@@ -385,6 +410,7 @@ def run_fv(args):
         "e2e": e2e, "cpu_baseline": cpu_baseline, "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "elementwise_ms_per_step": (ms_total / args.steps) - attn_avg_ms,
+        "vdn_window_attention": window,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -403,6 +429,7 @@ def parse(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=96, help="oracle query rows per head for cpu_baseline")
     ap.add_argument("--ref-rows", type=int, default=16, help="oracle query rows per head per reference step")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-window", action="store_true", help="skip the windowed-attention measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

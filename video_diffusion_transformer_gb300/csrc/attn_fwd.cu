@@ -354,9 +354,15 @@ template <bool kWindow>
 struct ColMask {
     int valid, a0, w0, w1, a1;
     bool all;
+    // Branch-free: every column costs the same few integer operations.
     __device__ __forceinline__ bool ok(int c) const {
         if (!kWindow) return c < valid;
-        return c < valid && (all || c < a0 || (c >= w0 && c < w1) || c >= a1);
+        const bool in_w = (unsigned)(c - w0) < (unsigned)(w1 - w0);
+        return (c < valid) & (all | (c < a0) | in_w | (c >= a1));
+    }
+    // No column of the tile is visible to this row.
+    __device__ __forceinline__ bool none() const {
+        return kWindow && !all && a0 <= 0 && (w1 <= 0 || w0 >= kRows) && a1 >= kRows;
     }
 };
 
@@ -443,12 +449,6 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
             ok = __all_sync(0xffffffffu, wait_bar(sm, kBarSFull + k, tile & 1u, p, kWhereSFull));
             if (!ok) break;
             ptx::tc_fence_after();
-            uint32_t s[4][32];
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) ptx::tmem_ld_32x32b_x32(t_s + (uint32_t)(32 * c4), s[c4]);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) ptx::reg_fence(s[c4]);
             const int kb = (kWindow ? kl.tile(j) : j) * kRows;
             ColMask<kWindow> cm;
             cm.valid = p.n - kb;
@@ -457,13 +457,36 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
             cm.w0 = rw.w0 - kb;
             cm.w1 = rw.w1 - kb;
             cm.a1 = last_begin - kb;
-            bool need = cm.valid < kRows;
-            if (kWindow && !cm.all)
-                need = need || !((cm.w0 <= 0 && cm.w1 >= kRows) || cm.a0 >= kRows || cm.a1 <= 0);
+            const bool row_none = cm.none();
+            if (kWindow && __all_sync(0xffffffffu, row_none)) {
+                // No row of this warp sees any key of the tile: zero probabilities,
+                // no scores read (never the first tile, which holds the first frame).
+                uint32_t zero[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) zero[i] = 0u;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) ptx::tmem_st_32x32b_x16(t_s + (uint32_t)(c4 * 16), zero);
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(sm.b(kBarPFull + k));
+                ++tile;
+                continue;
+            }
+            uint32_t s[4][32];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) ptx::tmem_ld_32x32b_x32(t_s + (uint32_t)(32 * c4), s[c4]);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) ptx::reg_fence(s[c4]);
+            // A row sees all of the tile, none of it, or part of it.  Only a
+            // partly visible row needs the per-column test; a row that sees
+            // none gets an infinite offset, so its probabilities are exact zeros.
+            const bool row_full = cm.valid >= kRows &&
+                                  (!kWindow || cm.all || (cm.w0 <= 0 && cm.w1 >= kRows) || cm.a0 >= kRows || cm.a1 <= 0);
             // one code path per warp: the tcgen05 copies are warp-collective
-            const bool masked = __any_sync(0xffffffffu, need);
-            const float m_tile =
-                (masked ? row_max<true, kWindow>(s, cm) : row_max<false, kWindow>(s, cm)) * p.scale_log2;
+            const bool masked = __any_sync(0xffffffffu, !row_full && !row_none);
+            float m_tile = (masked ? row_max<true, kWindow>(s, cm) : row_max<false, kWindow>(s, cm)) * p.scale_log2;
+            if (kWindow && row_none) m_tile = -INFINITY;
             float factor = 1.f;
             bool rescale = false;
             if (j == 0) {
@@ -473,8 +496,9 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
                 m_used = m_tile;
                 rescale = true;
             }
-            const float tile_sum = masked ? write_probs<true, kWindow>(s, cm, p.scale_log2, m_used, t_s)
-                                          : write_probs<false, kWindow>(s, cm, p.scale_log2, m_used, t_s);
+            const float m_eff = (kWindow && row_none) ? INFINITY : m_used;
+            const float tile_sum = masked ? write_probs<true, kWindow>(s, cm, p.scale_log2, m_eff, t_s)
+                                          : write_probs<false, kWindow>(s, cm, p.scale_log2, m_eff, t_s);
             l = l * factor + tile_sum;
             // O (complete through tile j-1, since S_j is) must carry the new maximum
             // before the next P.V accumulates into it.
