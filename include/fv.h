@@ -159,6 +159,31 @@ fv_status fv_gated_residual(const void *x, const void *a, void *out, int64_t N, 
                             int step, void *stream);
 
 /*
+ * Per-token modality rows ("FastH3 Preview v1", section "Update: consumer
+ * GPUs and Trim": the six modulation vectors exist per modality, indexed
+ * timestep_indices * 3 + token_tags).  The same two ops, but token i reads
+ * table row step * num_modalities + token_tags[i], so a packed
+ * [text | audio | video] sequence takes each token's own modality row.
+ *
+ * token_tags:     device uint8 [N], each in [0, num_modalities).  A tag out of
+ *                 range is not detected on the host: the kernel leaves that
+ *                 row's output unwritten and fv_sync_status() reports
+ *                 FV_ERR_ARG.
+ * num_modalities: 1 .. 255; tables hold num_steps * num_modalities rows.
+ * step:           0 .. num_steps-1, else FV_ERR_STEP.
+ * All other arguments, layouts and checks as the untagged calls.
+ */
+fv_status fv_adaln_modulate_tagged(const void *x, void *y, int y_is_fp32, int64_t N, int C,
+                                   const float *shift_table, const float *scale_table,
+                                   int64_t table_ld, int num_steps, int num_modalities, int step,
+                                   const uint8_t *token_tags, float eps, void *stream);
+
+fv_status fv_gated_residual_tagged(const void *x, const void *a, void *out, int64_t N, int C,
+                                   const float *gate_table, int64_t table_ld, int num_steps,
+                                   int num_modalities, int step, const uint8_t *token_tags,
+                                   void *stream);
+
+/*
  * Schedule cursor: the step whose stored timestep equals t exactly.
  * ladder: host float32 [num_steps].  Writes the first matching index to
  * *step_out and returns FV_OK, or returns FV_ERR_STEP if t is not on the
@@ -169,7 +194,8 @@ fv_status fv_step_for_timestep(const float *ladder, int num_steps, float t, int 
 /*
  * Synchronise `stream`, then read and clear the current device's status word.
  * Returns FV_OK, FV_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait
- * since the last call, or FV_ERR_LAUNCH if the stream reports a CUDA error.
+ * since the last call, FV_ERR_ARG if a kernel met an out-of-range token tag,
+ * or FV_ERR_LAUNCH if the stream reports a CUDA error.
  */
 fv_status fv_sync_status(void *stream);
 

@@ -141,3 +141,15 @@ def test_window_null_pointers(lib):
     assert lib.fv_attn_fwd_window(None, B, C, O, 4032, 4, 128, 0.088, 4, 1008, 5, 1, None, None) == -1
     assert lib.fv_attn_fwd_window(A, B, C, O, 4032, 4, 128, 0.088, 4, 1008, 5, 1, T + 2, None) == -3
     assert lib.fv_attn_fwd_window(A, B, C, O, 4032, 4, 128, 0.088, 4, 1008, 5, 1, A + 4, None) == -9
+
+
+def test_tagged_ops_reject_bad_arguments(lib):
+    # modulate: missing tags, zero modalities, off-ladder step
+    assert lib.fv_adaln_modulate_tagged(A, O, 0, 1008, 5376, B, C, 5376, 8, 3, 3, None, 1e-6, None) == -1
+    assert lib.fv_adaln_modulate_tagged(A, O, 0, 1008, 5376, B, C, 5376, 8, 0, 3, T, 1e-6, None) == -2
+    assert lib.fv_adaln_modulate_tagged(A, O, 0, 1008, 5376, B, C, 5376, 8, 256, 3, T, 1e-6, None) == -2
+    assert lib.fv_adaln_modulate_tagged(A, O, 0, 1008, 5376, B, C, 5376, 8, 3, 8, T, 1e-6, None) == -4
+    # gated residual
+    assert lib.fv_gated_residual_tagged(A, B, O, 5040, 5376, C, 5376, 8, 3, 3, None, None) == -1
+    assert lib.fv_gated_residual_tagged(A, B, O, 5040, 5376, C, 5376, 8, 3, -1, T, None) == -4
+    assert lib.fv_gated_residual_tagged(A, B, B, 5040, 5376, C, 5376, 8, 3, 3, T, None) == -9

@@ -150,3 +150,75 @@ def test_off_ladder_step_is_rejected():
     assert e.value.code == -4
     with pytest.raises(fv.FvError):
         fv.adaln_modulate(x, gate, gate, -1)
+
+
+def packed_tags(n, gen_seed=3, runs=(300, 200)):
+    """[text | audio | video] runs (tags 0, 1, 2), then a stretch of random tags."""
+    t = torch.full((n,), 2, dtype=torch.uint8)
+    t[:runs[0]] = 0
+    t[runs[0]:runs[0] + runs[1]] = 1
+    g = torch.Generator().manual_seed(gen_seed)
+    tail = n // 3
+    t[n - tail:] = torch.randint(0, 3, (tail,), generator=g).to(torch.uint8)
+    return t
+
+
+def test_modulate_tagged_rows():
+    n, c, m, steps = 1500, W.HIDDEN, 3, 8
+    x = W.randn_bf16((n, c), 11, "x")
+    g = torch.Generator().manual_seed(12)
+    shift = (torch.randn((steps * m, c), generator=g) * 0.1).float()
+    scale = (torch.randn((steps * m, c), generator=g) * 0.1).float()
+    tags = packed_tags(n)
+    y = fv.adaln_modulate_tagged(x.cuda(), shift.cuda(), scale.cuda(), STEP, tags.cuda(), m, eps=EPS,
+                                 out_dtype=torch.float32)
+    fv.sync_status()
+    y = y.cpu().numpy()
+    for tag in range(m):
+        rows = np.nonzero(tags.numpy() == tag)[0]
+        ref = oracle.modulate(x, shift[STEP * m + tag].numpy(), scale[STEP * m + tag].numpy(), EPS, rows=rows)
+        rel = np.abs(y[rows] - ref) / np.maximum(1.0, np.abs(ref))
+        assert rel.max() <= P.MODULATE_REL, (tag, rel.max())
+
+
+def test_gated_residual_tagged_rows():
+    n, c, m, steps = 1500, W.HIDDEN, 3, 8
+    x = W.randn_bf16((n, c), 13, "x")
+    a = W.randn_bf16((n, c), 13, "a")
+    gate = (torch.randn((steps * m, c), generator=torch.Generator().manual_seed(14)) * 0.1).float()
+    tags = packed_tags(n, 5)
+    out = fv.gated_residual_tagged(x.cuda(), a.cuda(), gate.cuda(), STEP, tags.cuda(), m).cpu()
+    fv.sync_status()
+    for tag in range(m):
+        rows = np.nonzero(tags.numpy() == tag)[0]
+        _, ref_bits = oracle.gated_residual(x, a, gate[STEP * m + tag].numpy(), rows=rows)
+        assert P.ulp_distance(P.bf16_bits(out[rows]), ref_bits).max() <= 1
+
+
+def test_single_modality_tags_equal_untagged_call():
+    w = W.WORKLOADS["clip17_5040"]
+    x, a, gate = W.gated_residual_inputs(w, rows=700)
+    tags = torch.zeros(700, dtype=torch.uint8).cuda()
+    o1 = fv.gated_residual_tagged(x.cuda(), a.cuda(), gate.cuda(), STEP, tags, 1)
+    o2 = fv.gated_residual(x.cuda(), a.cuda(), gate.cuda(), STEP)
+    xm, sh, sc = W.modulate_inputs(w, rows=700)
+    y1 = fv.adaln_modulate_tagged(xm.cuda(), sh.cuda(), sc.cuda(), STEP, tags, 1, out_dtype=torch.float32)
+    y2 = fv.adaln_modulate(xm.cuda(), sh.cuda(), sc.cuda(), STEP, out_dtype=torch.float32)
+    fv.sync_status()
+    assert torch.equal(o1, o2)
+    assert float((y1 - y2).abs().max()) <= 1e-6
+
+
+def test_out_of_range_tag_is_reported_and_context_survives():
+    n, c = 64, 256
+    x = torch.zeros((n, c), dtype=torch.bfloat16, device="cuda")
+    gate = torch.zeros((2 * 3, c), dtype=torch.float32, device="cuda")
+    tags = torch.full((n,), 3, dtype=torch.uint8, device="cuda")  # 3 modalities: tags 0..2
+    fv.gated_residual_tagged(x, x.clone(), gate, 1, tags, 3)
+    with pytest.raises(fv.FvError) as e:
+        fv.sync_status()
+    assert e.value.code == -8
+    fv.sync_status()  # cleared
+    tags.fill_(1)
+    fv.gated_residual_tagged(x, x.clone(), gate, 1, tags, 3)
+    fv.sync_status()

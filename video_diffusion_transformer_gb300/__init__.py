@@ -24,7 +24,8 @@ STATUS = {
 }
 # every symbol include/fv.h declares
 EXPORTS = ("fv_attn_fwd", "fv_adaln_modulate", "fv_gated_residual", "fv_step_for_timestep", "fv_sync_status",
-           "fv_status_string", "fv_version", "fv_attn_fwd_noalloc", "fv_attn_fwd_window")
+           "fv_status_string", "fv_version", "fv_attn_fwd_noalloc", "fv_attn_fwd_window",
+           "fv_adaln_modulate_tagged", "fv_gated_residual_tagged")
 NOALLOC_MAX_LAUNCHES = 64
 
 HEAD_DIM = 128
@@ -59,6 +60,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fv_adaln_modulate.restype = i32
     lib.fv_gated_residual.argtypes = [vp, vp, vp, i64, i32, vp, i64, i32, i32, vp]
     lib.fv_gated_residual.restype = i32
+    lib.fv_adaln_modulate_tagged.argtypes = [vp, vp, i32, i64, i32, vp, vp, i64, i32, i32, i32, vp, f32, vp]
+    lib.fv_adaln_modulate_tagged.restype = i32
+    lib.fv_gated_residual_tagged.argtypes = [vp, vp, vp, i64, i32, vp, i64, i32, i32, i32, vp, vp]
+    lib.fv_gated_residual_tagged.restype = i32
     lib.fv_step_for_timestep.argtypes = [ctypes.POINTER(ctypes.c_float), i32, f32, ctypes.POINTER(ctypes.c_int)]
     lib.fv_step_for_timestep.restype = i32
     lib.fv_sync_status.argtypes = [vp]
@@ -222,6 +227,48 @@ def gated_residual(x: torch.Tensor, a: torch.Tensor, gate_table: torch.Tensor, s
         _dev(x, "x", torch.bfloat16), _dev(a, "a", torch.bfloat16), _dev(out, "out", torch.bfloat16), n, c,
         gate_table.data_ptr(), gate_table.stride(0), gate_table.shape[0], int(step), _stream_ptr(stream))
     _check(code, "fv_gated_residual")
+    return out
+
+
+def adaln_modulate_tagged(x: torch.Tensor, shift_table: torch.Tensor, scale_table: torch.Tensor, step: int,
+                          tags: torch.Tensor, num_modalities: int, *, eps: float = 1e-6,
+                          out: torch.Tensor | None = None, out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    """Modulate with per-token modality rows: token i reads table row
+    step * num_modalities + tags[i] (tables float32 [steps * num_modalities, C])."""
+    n, c = x.shape
+    if out is None:
+        out = torch.empty((n, c), dtype=out_dtype, device=x.device)
+    if shift_table.shape != scale_table.shape or shift_table.dim() != 2 or shift_table.stride(1) != 1 \
+            or scale_table.stride(1) != 1:
+        raise ValueError("tables must be float32 [steps * modalities, ld] with contiguous rows")
+    if shift_table.shape[0] % num_modalities:
+        raise ValueError("table rows must be steps * num_modalities")
+    if tags.shape != (n,):
+        raise ValueError("tags must be uint8 [N]")
+    code = load_library().fv_adaln_modulate_tagged(
+        _dev(x, "x", torch.bfloat16), _dev(out, "out", out.dtype), 1 if out.dtype == torch.float32 else 0, n, c,
+        shift_table.data_ptr(), scale_table.data_ptr(), shift_table.stride(0), shift_table.shape[0] // num_modalities,
+        int(num_modalities), int(step), _dev(tags, "tags", torch.uint8), float(eps), _stream_ptr(stream))
+    _check(code, "fv_adaln_modulate_tagged")
+    return out
+
+
+def gated_residual_tagged(x: torch.Tensor, a: torch.Tensor, gate_table: torch.Tensor, step: int,
+                          tags: torch.Tensor, num_modalities: int, *, out: torch.Tensor | None = None,
+                          stream=None) -> torch.Tensor:
+    """Gated residual with per-token modality rows of the gate table."""
+    n, c = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    if gate_table.dim() != 2 or gate_table.stride(1) != 1 or gate_table.shape[0] % num_modalities:
+        raise ValueError("gate_table must be float32 [steps * modalities, ld] with contiguous rows")
+    if tags.shape != (n,):
+        raise ValueError("tags must be uint8 [N]")
+    code = load_library().fv_gated_residual_tagged(
+        _dev(x, "x", torch.bfloat16), _dev(a, "a", torch.bfloat16), _dev(out, "out", torch.bfloat16), n, c,
+        gate_table.data_ptr(), gate_table.stride(0), gate_table.shape[0] // num_modalities, int(num_modalities),
+        int(step), _dev(tags, "tags", torch.uint8), _stream_ptr(stream))
+    _check(code, "fv_gated_residual_tagged")
     return out
 
 

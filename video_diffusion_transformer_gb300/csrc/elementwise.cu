@@ -174,6 +174,132 @@ __global__ void __launch_bounds__(kEwThreads) gated_residual_kernel(const uint4 
     }
 }
 
+// Per-token modality rows: token i reads table row row_base + tags[i] (the
+// pages index the AdaLN table by timestep * 3 + token tag).  Table rows are
+// read through the read-only cache; a tag >= num_tags skips the row and
+// records kDevBadTag in the status word.
+template <int kChunks>
+__global__ void __launch_bounds__(kEwThreads, kChunks <= 21 ? 2 : 1)
+    modulate_tagged_kernel(const uint4 *__restrict__ x, void *__restrict__ y, int y_fp32, int64_t n, int c,
+                           const float *__restrict__ shift_base, const float *__restrict__ scale_base, int64_t ld,
+                           int row_base, const uint8_t *__restrict__ tags, int num_tags, float eps, int *status) {
+    const int lane = (int)(threadIdx.x & 31);
+    const int cq = c >> 3;
+    for (int64_t row = (int64_t)blockIdx.x * kEwWarps + (threadIdx.x >> 5); row < n;
+         row += (int64_t)gridDim.x * kEwWarps) {
+        const int tag = (int)__ldg(tags + row);
+        if (tag >= num_tags) {
+            if (lane == 0) atomicCAS(status, 0, kDevBadTag);
+            continue;
+        }
+        const float4 *sh4 = reinterpret_cast<const float4 *>(shift_base + (int64_t)(row_base + tag) * ld);
+        const float4 *sc4 = reinterpret_cast<const float4 *>(scale_base + (int64_t)(row_base + tag) * ld);
+        const uint4 *xr = x + row * cq;
+        uint4 v[kChunks];
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+            const int q = lane + 32 * i;
+            v[i] = q < cq ? __ldcs(xr + q) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+            float f[8];
+            unpack8_fresh(v[i], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s += f[e];
+        }
+        const float mu = warp_sum(s) / (float)c;
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+            if (lane + 32 * i < cq) {
+                float f[8];
+                unpack8_fresh(v[i], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float d = f[e] - mu;
+                    ss = fmaf(d, d, ss);
+                }
+            }
+        }
+        const float rstd = 1.0f / sqrtf(warp_sum(ss) / (float)c + eps);
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+            const int q = lane + 32 * i;
+            if (q < cq) {
+                float f[8];
+                unpack8_fresh(v[i], f);
+                const float4 a0 = __ldg(sh4 + 2 * q), a1 = __ldg(sh4 + 2 * q + 1);
+                const float4 b0 = __ldg(sc4 + 2 * q), b1 = __ldg(sc4 + 2 * q + 1);
+                const float sh[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float sc[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                float r[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) r[e] = fmaf((f[e] - mu) * rstd, 1.0f + sc[e], sh[e]);
+                if (y_fp32) {
+                    float4 *yr = reinterpret_cast<float4 *>(y) + row * (int64_t)(2 * cq) + 2 * q;
+                    __stcs(yr, make_float4(r[0], r[1], r[2], r[3]));
+                    __stcs(yr + 1, make_float4(r[4], r[5], r[6], r[7]));
+                } else {
+                    uint4 w;
+                    w.x = pack_bf16x2(r[0], r[1]);
+                    w.y = pack_bf16x2(r[2], r[3]);
+                    w.z = pack_bf16x2(r[4], r[5]);
+                    w.w = pack_bf16x2(r[6], r[7]);
+                    __stcs(reinterpret_cast<uint4 *>(y) + row * cq + q, w);
+                }
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kEwThreads)
+    gated_residual_tagged_kernel(const uint4 *x, const uint4 *__restrict__ a, uint4 *out, int64_t n, int cq,
+                                 const float *__restrict__ gate_base, int64_t ld, int row_base,
+                                 const uint8_t *__restrict__ tags, int num_tags, int *status) {
+    constexpr int kBatch = 8;
+    const int lane = (int)(threadIdx.x & 31);
+    for (int64_t row = (int64_t)blockIdx.x * kEwWarps + (threadIdx.x >> 5); row < n;
+         row += (int64_t)gridDim.x * kEwWarps) {
+        const int tag = (int)__ldg(tags + row);
+        if (tag >= num_tags) {
+            if (lane == 0) atomicCAS(status, 0, kDevBadTag);
+            continue;
+        }
+        const float4 *gate = reinterpret_cast<const float4 *>(gate_base + (int64_t)(row_base + tag) * ld);
+        const int64_t base = row * cq;
+        for (int q0 = 0; q0 < cq; q0 += 32 * kBatch) {
+            uint4 xv[kBatch], av[kBatch];
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                const int q = q0 + lane + 32 * i;
+                if (q < cq) {
+                    xv[i] = __ldcs(x + base + q);
+                    av[i] = __ldcs(a + base + q);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                const int q = q0 + lane + 32 * i;
+                if (q < cq) {
+                    float fx[8], fa[8];
+                    unpack8(xv[i], fx);
+                    unpack8(av[i], fa);
+                    const float4 g0 = __ldg(gate + 2 * q), g1 = __ldg(gate + 2 * q + 1);
+                    const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                    uint4 w;
+                    w.x = pack_bf16x2(fmaf(g[0], fa[0], fx[0]), fmaf(g[1], fa[1], fx[1]));
+                    w.y = pack_bf16x2(fmaf(g[2], fa[2], fx[2]), fmaf(g[3], fa[3], fx[3]));
+                    w.z = pack_bf16x2(fmaf(g[4], fa[4], fx[4]), fmaf(g[5], fa[5], fx[5]));
+                    w.w = pack_bf16x2(fmaf(g[6], fa[6], fx[6]), fmaf(g[7], fa[7], fx[7]));
+                    __stcs(out + base + q, w);
+                }
+            }
+        }
+    }
+}
+
 template <int kChunks>
 fv_status launch_modulate_t(const void *x, void *y, bool y_fp32, int64_t n, int c, const float *shift_row,
                             const float *scale_row, float eps, int num_sms, cudaStream_t stream) {
@@ -195,7 +321,51 @@ fv_status launch_modulate_t(const void *x, void *y, bool y_fp32, int64_t n, int 
     return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
 }
 
+template <int kChunks>
+fv_status launch_modulate_tagged_t(const TaggedRows &t, const void *x, void *y, bool y_fp32, int64_t n, int c,
+                                   float eps, int num_sms, cudaStream_t stream) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, modulate_tagged_kernel<kChunks>, kEwThreads, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
+        return FV_ERR_LAUNCH;
+    const int64_t need = (n + kEwWarps - 1) / kEwWarps;
+    const int64_t full = (int64_t)num_sms * per_sm;
+    const int grid = (int)(need < full ? need : full);
+    modulate_tagged_kernel<kChunks><<<grid, kEwThreads, 0, stream>>>(
+        static_cast<const uint4 *>(x), y, y_fp32 ? 1 : 0, n, c, t.table0, t.table1, t.ld, t.row_base, t.tags,
+        t.num_tags, eps, t.status);
+    return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
+}
+
 }  // namespace
+
+fv_status launch_adaln_modulate_tagged(const TaggedRows &t, const void *x, void *y, bool y_fp32, int64_t n, int c,
+                                       float eps, int num_sms, cudaStream_t stream) {
+    const int chunks = (c / 8 + 31) / 32;
+    if (chunks <= 4) return launch_modulate_tagged_t<4>(t, x, y, y_fp32, n, c, eps, num_sms, stream);
+    if (chunks <= 8) return launch_modulate_tagged_t<8>(t, x, y, y_fp32, n, c, eps, num_sms, stream);
+    if (chunks <= 16) return launch_modulate_tagged_t<16>(t, x, y, y_fp32, n, c, eps, num_sms, stream);
+    if (chunks <= 21) return launch_modulate_tagged_t<21>(t, x, y, y_fp32, n, c, eps, num_sms, stream);
+    if (chunks <= 32) return launch_modulate_tagged_t<32>(t, x, y, y_fp32, n, c, eps, num_sms, stream);
+    return FV_ERR_SHAPE;
+}
+
+fv_status launch_gated_residual_tagged(const TaggedRows &t, const void *x, const void *a, void *out, int64_t n,
+                                       int c, int num_sms, cudaStream_t stream) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gated_residual_tagged_kernel, kEwThreads, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
+        return FV_ERR_LAUNCH;
+    const int64_t need = (n + kEwWarps - 1) / kEwWarps;
+    const int64_t full = (int64_t)num_sms * per_sm;
+    const int grid = (int)(need < full ? need : full);
+    gated_residual_tagged_kernel<<<grid, kEwThreads, 0, stream>>>(
+        static_cast<const uint4 *>(x), static_cast<const uint4 *>(a), static_cast<uint4 *>(out), n, c / 8, t.table0,
+        t.ld, t.row_base, t.tags, t.num_tags, t.status);
+    return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
+}
 
 fv_status launch_adaln_modulate(const void *x, void *y, bool y_fp32, int64_t n, int c, const float *shift_row,
                                 const float *scale_row, float eps, int num_sms, cudaStream_t stream) {

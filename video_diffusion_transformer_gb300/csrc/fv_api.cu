@@ -164,6 +164,49 @@ fv_status fv_gated_residual(const void *x, const void *a, void *out, int64_t N, 
                                      static_cast<cudaStream_t>(stream));
 }
 
+fv_status fv_adaln_modulate_tagged(const void *x, void *y, int y_is_fp32, int64_t N, int C, const float *shift_table,
+                                   const float *scale_table, int64_t table_ld, int num_steps, int num_modalities,
+                                   int step, const uint8_t *token_tags, float eps, void *stream) {
+    if (!x || !y || !shift_table || !scale_table || !token_tags) return FV_ERR_NULL;
+    if (N < 1 || C < 8 || C > 8192 || (C % 8) != 0 || table_ld < C || num_steps < 1 || num_modalities < 1 ||
+        num_modalities > 255)
+        return FV_ERR_SHAPE;
+    if (step < 0 || step >= num_steps) return FV_ERR_STEP;
+    if (!std::isfinite(eps) || eps < 0.0f) return FV_ERR_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(shift_table, 16) || !aligned(scale_table, 16) ||
+        (table_ld % 4) != 0)
+        return FV_ERR_ALIGN;
+    const size_t xb = (size_t)N * (size_t)C * 2u, yb = (size_t)N * (size_t)C * (y_is_fp32 ? 4u : 2u);
+    if (overlaps(x, xb, y, yb)) return FV_ERR_ALIAS;
+    DeviceState *d = nullptr;
+    fv_status st = device_state(&d);
+    if (st != FV_OK) return st;
+    fv::TaggedRows t{shift_table, scale_table, table_ld, step * num_modalities, token_tags, num_modalities,
+                     d->status};
+    return fv::launch_adaln_modulate_tagged(t, x, y, y_is_fp32 != 0, N, C, eps, d->num_sms,
+                                            static_cast<cudaStream_t>(stream));
+}
+
+fv_status fv_gated_residual_tagged(const void *x, const void *a, void *out, int64_t N, int C, const float *gate_table,
+                                   int64_t table_ld, int num_steps, int num_modalities, int step,
+                                   const uint8_t *token_tags, void *stream) {
+    if (!x || !a || !out || !gate_table || !token_tags) return FV_ERR_NULL;
+    if (N < 1 || C < 8 || C > (1 << 20) || (C % 8) != 0 || table_ld < C || num_steps < 1 || num_modalities < 1 ||
+        num_modalities > 255)
+        return FV_ERR_SHAPE;
+    if (step < 0 || step >= num_steps) return FV_ERR_STEP;
+    if (!aligned(x, 16) || !aligned(a, 16) || !aligned(out, 16) || !aligned(gate_table, 16) || (table_ld % 4) != 0)
+        return FV_ERR_ALIGN;
+    const size_t b = (size_t)N * (size_t)C * 2u;
+    if (overlaps(out, b, a, b)) return FV_ERR_ALIAS;
+    if (out != x && overlaps(out, b, x, b)) return FV_ERR_ALIAS;
+    DeviceState *d = nullptr;
+    fv_status st = device_state(&d);
+    if (st != FV_OK) return st;
+    fv::TaggedRows t{gate_table, nullptr, table_ld, step * num_modalities, token_tags, num_modalities, d->status};
+    return fv::launch_gated_residual_tagged(t, x, a, out, N, C, d->num_sms, static_cast<cudaStream_t>(stream));
+}
+
 fv_status fv_step_for_timestep(const float *ladder, int num_steps, float t, int *step_out) {
     if (!ladder || !step_out) return FV_ERR_NULL;
     if (num_steps < 1) return FV_ERR_SHAPE;
@@ -189,7 +232,7 @@ fv_status fv_sync_status(void *stream) {
     if (word != 0) {
         if (cudaMemsetAsync(d->status, 0, sizeof(int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
             return FV_ERR_LAUNCH;
-        return FV_ERR_DEVICE_TIMEOUT;
+        return (word & 0xFF00) == fv::kDevBadTag ? FV_ERR_ARG : FV_ERR_DEVICE_TIMEOUT;
     }
     return FV_OK;
 }

@@ -11,6 +11,8 @@ namespace fv {
 // Device status word values (0 = no error).  A kernel that gives up on a
 // bounded wait stores kDevTimeout | where, where names the wait.
 constexpr int kDevTimeout = 0x7100;
+// A per-token modality tag was >= the number of modalities; the row was skipped.
+constexpr int kDevBadTag = 0x7200;
 
 struct AttnLaunch {
     const void *q, *k, *v;
@@ -35,5 +37,22 @@ fv_status launch_adaln_modulate(const void *x, void *y, bool y_fp32, int64_t n, 
 
 fv_status launch_gated_residual(const void *x, const void *a, void *out, int64_t n, int c, const float *gate_row,
                                 int num_sms, cudaStream_t stream);
+
+// Table rows chosen per token: token i reads row row_base + tags[i] of
+// table0 (and table1), rows ld floats apart.
+struct TaggedRows {
+    const float *table0, *table1;
+    int64_t ld;
+    int row_base;
+    const uint8_t *tags;
+    int num_tags;
+    int *status;
+};
+
+fv_status launch_adaln_modulate_tagged(const TaggedRows &t, const void *x, void *y, bool y_fp32, int64_t n, int c,
+                                       float eps, int num_sms, cudaStream_t stream);
+
+fv_status launch_gated_residual_tagged(const TaggedRows &t, const void *x, const void *a, void *out, int64_t n,
+                                       int c, int num_sms, cudaStream_t stream);
 
 }  // namespace fv
