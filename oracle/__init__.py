@@ -22,6 +22,7 @@ import os
 import numpy as np
 
 from . import build as _build
+from . import delta  # noqa: F401  (fp64 Video Delta Attention, numpy)
 
 
 def default_threads() -> int:
