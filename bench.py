@@ -308,6 +308,43 @@ def run_fv(args):
                       "effective_tflops": 4.0 * W.HEAD_DIM * w.heads * pairs / (wms / 1e3) / 1e12,
                       "speedup_vs_dense": (sum(attn_ms) / len(attn_ms)) / wms}
 
+        # ---- Video Delta Attention (the VDN linear branch) on the same Q, K, V
+        delta = None
+        if not args.no_window and w.n % W.tokens_per_latent_frame(1344, 768) == 0:
+            t_f = W.tokens_per_latent_frame(1344, 768)
+            frames = w.n // t_f
+            gd = torch.Generator(device="cpu").manual_seed(77)
+            beta = torch.sigmoid(torch.randn((w.heads, w.n), generator=gd)).to(dev)
+            alpha = (0.9 + 0.1 * torch.rand((w.heads, frames, W.HEAD_DIM), generator=gd)).to(dev)
+            tstate = (torch.randn((w.heads, W.HEAD_DIM, W.HEAD_DIM), generator=gd) * 0.1).to(dev)
+            od = torch.empty_like(q)
+            st_shape = (2, w.heads, frames, W.HEAD_DIM, W.HEAD_DIM)
+            states = torch.empty(st_shape, dtype=torch.float32, device=dev)
+            wsp = torch.empty(st_shape, dtype=torch.float32, device=dev)
+
+            def run_delta():
+                fv.delta_attn(q, k, v, beta, alpha, frame_tokens=t_f, chunk_frames=5, window_chunks=1,
+                              text_state=tstate, out=od, states=states, workspace=wsp, stream=stream)
+
+            run_delta()
+            reps = 5
+            d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            d0.record(stream)
+            for _ in range(reps):
+                run_delta()
+            d1.record(stream)
+            torch.cuda.synchronize(dev)
+            fv.sync_status(stream)
+            dms = d0.elapsed_time(d1) / reps
+            dd = W.HEAD_DIM
+            written = max(0, frames - 2)
+            flops = w.heads * (written * (4.0 * t_f * dd * dd + 4.3 * dd ** 3 + 2 * 2.0 * dd ** 3)
+                               + frames * 2.0 * t_f * dd * dd)
+            delta = {"kernels": "vda_stats, vda_solve, vda_scan, vda_readout (float32)", "ms": dms,
+                     "gflop": flops / 1e9, "tflops": flops / (dms / 1e3) / 1e12,
+                     "vdn_hybrid_ms": (window["ms"] + dms) if window else None}
+
         # ---- end to end through the C ABI: pinned host inputs in, results out.
         # Every step copies its own inputs host->device and reads its results
         # back; copies run on their own streams, double-buffered, so step i's
@@ -411,6 +448,7 @@ def run_fv(args):
         "clocks": clocks,
         "elementwise_ms_per_step": (ms_total / args.steps) - attn_avg_ms,
         "vdn_window_attention": window,
+        "vdn_delta_attention": delta,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

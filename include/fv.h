@@ -120,6 +120,41 @@ fv_status fv_attn_fwd_window(const void *Q, const void *K, const void *V, void *
                              float *lse, void *stream);
 
 /*
+ * Video Delta Attention: the linear branch of Video DeltaNet ("FreeVideo",
+ * section "Where Video DeltaNet comes in").  Per head, q and k are
+ * L2-normalised; frame t (frame_tokens tokens) has
+ *   A_t = sum_u beta_u k_u k_u^T,   B_t = sum_u beta_u v_u k_u^T,
+ * and the state after writing it is the closed form of the frame's joint
+ * least-squares write,
+ *   S_t = (S_{t-1} Diag(alpha_t) + B_t) (I + A_t)^{-1}.
+ * Two scans run, forward over frames 1 .. F-2 and reverse over F-2 .. 1, each
+ * seeded with text_state / 2; frames 0 and F-1 (the softmax branch's global
+ * anchors) are not written.  A token of chunk c = frame / chunk_frames reads
+ *   o = (S_fwd[p] + S_rev[n]) q,  p = max((c - window_chunks) chunk_frames - 1, 0),
+ *                                n = min((c + window_chunks + 1) chunk_frames, F - 1),
+ * the states just before and just after its softmax window (fv_attn_fwd_window).
+ *
+ * Q, K, V:      device bf16 [N, H*128], as fv_attn_fwd; O: device bf16 [N, H*128]
+ *               (the linear branch's output, before its gate and projection).
+ * beta:         device float32 [H, N], write strengths, >= 0.
+ * alpha:        device float32 [H, F, 128], per-frame per-channel decay (entries
+ *               of frames 0 and F-1 are not read).
+ * text_state:   device float32 [H, 128, 128], or NULL for a zero state.
+ * states:       device float32 [2, H, F, 128, 128]: written with the forward
+ *               states (index 0) and reverse states (index 1) of every frame;
+ *               S_fwd[0] = S_rev[F-1] = text_state / 2.
+ * workspace:    device float32 [2, H, F, 128, 128], caller-owned scratch.
+ * N = F * frame_tokens; F >= 1; chunk_frames >= 1; window_chunks >= 0; D = 128;
+ * H 1 .. 256; all pointers 16-byte aligned; else FV_ERR_SHAPE / _NULL / _ALIGN.
+ * Compute: float32 throughout (normalisation, sums, a Cholesky solve per frame,
+ * the scans, the readout); O rounded once to bf16.
+ */
+fv_status fv_delta_attn(const void *Q, const void *K, const void *V, const float *beta,
+                        const float *alpha, const float *text_state, int64_t N, int H, int D,
+                        int frame_tokens, int chunk_frames, int window_chunks, void *O,
+                        float *states, float *workspace, void *stream);
+
+/*
  * Cached-AdaLN modulated LayerNorm of the residual stream for one schedule step:
  *   mu = mean_c x[i,c],  var = mean_c (x[i,c] - mu)^2   (biased)
  *   y[i,c] = (x[i,c] - mu) / sqrt(var + eps) * (1 + scale_table[step*ld + c])

@@ -25,7 +25,7 @@ STATUS = {
 # every symbol include/fv.h declares
 EXPORTS = ("fv_attn_fwd", "fv_adaln_modulate", "fv_gated_residual", "fv_step_for_timestep", "fv_sync_status",
            "fv_status_string", "fv_version", "fv_attn_fwd_noalloc", "fv_attn_fwd_window",
-           "fv_adaln_modulate_tagged", "fv_gated_residual_tagged")
+           "fv_adaln_modulate_tagged", "fv_gated_residual_tagged", "fv_delta_attn")
 NOALLOC_MAX_LAUNCHES = 64
 
 HEAD_DIM = 128
@@ -56,6 +56,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fv_attn_fwd.restype = i32
     lib.fv_attn_fwd_window.argtypes = [vp, vp, vp, vp, i64, i32, i32, f32, i32, i32, i32, i32, vp, vp]
     lib.fv_attn_fwd_window.restype = i32
+    lib.fv_delta_attn.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, vp, vp, vp, vp]
+    lib.fv_delta_attn.restype = i32
     lib.fv_adaln_modulate.argtypes = [vp, vp, i32, i64, i32, vp, vp, i64, i32, i32, f32, vp]
     lib.fv_adaln_modulate.restype = i32
     lib.fv_gated_residual.argtypes = [vp, vp, vp, i64, i32, vp, i64, i32, i32, vp]
@@ -158,6 +160,46 @@ def attn_fwd_window(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torc
                                              _stream_ptr(stream))
     _check(code, "fv_attn_fwd_window")
     return out
+
+
+def delta_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, alpha: torch.Tensor, *,
+               frame_tokens: int, chunk_frames: int = 5, window_chunks: int = 1,
+               text_state: torch.Tensor | None = None, out: torch.Tensor | None = None,
+               states: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+               stream=None):
+    """Video Delta Attention (the Video DeltaNet linear branch).
+
+    q, k, v: bf16 [N, H*128]; beta: float32 [H, N]; alpha: float32 [H, F, 128];
+    text_state: float32 [H, 128, 128] or None.  Returns (O bf16 [N, H*128],
+    states float32 [2, H, F, 128, 128]).  ``workspace`` (float32, same shape as
+    states) may be passed to avoid an allocation per call.
+    """
+    n = q.shape[0]
+    h = (q.numel() // max(1, n)) // HEAD_DIM
+    frames = n // frame_tokens
+    if k.shape != q.shape or v.shape != q.shape or beta.shape != (h, n) or alpha.shape != (h, frames, HEAD_DIM):
+        raise ValueError("shapes: q, k, v [N, H*128]; beta [H, N]; alpha [H, F, 128]")
+    shape = (2, h, frames, HEAD_DIM, HEAD_DIM)
+    if out is None:
+        out = torch.empty_like(q)
+    if states is None:
+        states = torch.empty(shape, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(shape, dtype=torch.float32, device=q.device)
+    if states.shape != shape or workspace.shape != shape:
+        raise ValueError("states and workspace must be float32 [2, H, F, 128, 128]")
+    ts = None
+    if text_state is not None:
+        if text_state.shape != (h, HEAD_DIM, HEAD_DIM):
+            raise ValueError("text_state must be float32 [H, 128, 128]")
+        ts = _dev(text_state, "text_state", torch.float32)
+    code = load_library().fv_delta_attn(
+        _dev(q, "q", torch.bfloat16), _dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16),
+        _dev(beta, "beta", torch.float32), _dev(alpha, "alpha", torch.float32), ts, n, h, HEAD_DIM,
+        int(frame_tokens), int(chunk_frames), int(window_chunks), _dev(out, "out", torch.bfloat16),
+        _dev(states, "states", torch.float32), _dev(workspace, "workspace", torch.float32), _stream_ptr(stream))
+    _check(code, "fv_delta_attn")
+    return out, states
 
 
 def attn_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor | None = None, *,

@@ -127,6 +127,42 @@ fv_status fv_attn_fwd_window(const void *Q, const void *K, const void *V, void *
                        stream);
 }
 
+fv_status fv_delta_attn(const void *Q, const void *K, const void *V, const float *beta, const float *alpha,
+                        const float *text_state, int64_t N, int H, int D, int frame_tokens, int chunk_frames,
+                        int window_chunks, void *O, float *states, float *workspace, void *stream) {
+    if (!Q || !K || !V || !beta || !alpha || !O || !states || !workspace) return FV_ERR_NULL;
+    if (D != 128 || N < 1 || N >= (int64_t(1) << 31) || H < 1 || H > 256 || frame_tokens < 1 ||
+        (N % frame_tokens) != 0 || chunk_frames < 1 || window_chunks < 0)
+        return FV_ERR_SHAPE;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(beta, 16) ||
+        !aligned(alpha, 16) || !aligned(states, 16) || !aligned(workspace, 16) ||
+        (text_state && !aligned(text_state, 16)))
+        return FV_ERR_ALIGN;
+    const size_t act = (size_t)N * (size_t)H * 128u * 2u;
+    if (overlaps(O, act, Q, act) || overlaps(O, act, K, act) || overlaps(O, act, V, act)) return FV_ERR_ALIAS;
+    const size_t st_bytes = (size_t)2 * H * (size_t)(N / frame_tokens) * 128u * 128u * 4u;
+    if (overlaps(states, st_bytes, workspace, st_bytes)) return FV_ERR_ALIAS;
+    DeviceState *d = nullptr;
+    fv_status st = device_state(&d);
+    if (st != FV_OK) return st;
+    fv::DeltaLaunch a;
+    a.q = Q;
+    a.k = K;
+    a.v = V;
+    a.beta = beta;
+    a.alpha = alpha;
+    a.text_state = text_state;
+    a.n = N;
+    a.heads = H;
+    a.frame_tokens = frame_tokens;
+    a.chunk_frames = chunk_frames;
+    a.window_chunks = window_chunks;
+    a.o = O;
+    a.states = states;
+    a.workspace = workspace;
+    return fv::launch_delta_attn(a, static_cast<cudaStream_t>(stream));
+}
+
 fv_status fv_adaln_modulate(const void *x, void *y, int y_is_fp32, int64_t N, int C, const float *shift_table,
                             const float *scale_table, int64_t table_ld, int num_steps, int step, float eps,
                             void *stream) {

@@ -49,6 +49,22 @@ struct TaggedRows {
     int *status;
 };
 
+struct DeltaLaunch {
+    const void *q, *k, *v;        // bf16 [n, heads * 128]
+    const float *beta;            // [heads, n]
+    const float *alpha;           // [heads, frames, 128]
+    const float *text_state;      // [heads, 128, 128] or null
+    int64_t n;
+    int heads;
+    int frame_tokens, chunk_frames, window_chunks;
+    void *o;                      // bf16 [n, heads * 128]
+    float *states;                // [2, heads, frames, 128, 128]
+    float *workspace;             // [2, heads, frames, 128, 128]
+};
+
+// Enqueue the Video Delta Attention kernels (stats, solve, scan, readout).
+fv_status launch_delta_attn(const DeltaLaunch &a, cudaStream_t stream);
+
 fv_status launch_adaln_modulate_tagged(const TaggedRows &t, const void *x, void *y, bool y_fp32, int64_t n, int c,
                                        float eps, int num_sms, cudaStream_t stream);
 
