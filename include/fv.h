@@ -146,7 +146,7 @@ fv_status fv_attn_fwd_window(const void *Q, const void *K, const void *V, void *
  * workspace:    device float32 [2, H, F, 128, 128], caller-owned scratch.
  * N = F * frame_tokens; F >= 1; chunk_frames >= 1; window_chunks >= 0; D = 128;
  * H 1 .. 256; all pointers 16-byte aligned; else FV_ERR_SHAPE / _NULL / _ALIGN.
- * Compute: float32 throughout (normalisation, sums, a Cholesky solve per frame,
+ * Compute: float32 throughout (normalisation, sums, a Gauss-Jordan solve per frame,
  * the scans, the readout); O rounded once to bf16.
  */
 fv_status fv_delta_attn(const void *Q, const void *K, const void *V, const float *beta,
