@@ -23,6 +23,7 @@ import numpy as np
 
 from . import build as _build
 from . import delta  # noqa: F401  (fp64 Video Delta Attention, numpy)
+from . import vsa  # noqa: F401  (VSA-style block-sparse attention, numpy)
 
 
 def default_threads() -> int:
