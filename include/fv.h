@@ -155,6 +155,52 @@ fv_status fv_delta_attn(const void *Q, const void *K, const void *V, const float
                         float *states, float *workspace, void *stream);
 
 /*
+ * VSA-style block-sparse attention ("FastH3 Preview v1", section "Lever two:
+ * VSA-H3 makes each of the four calls cheaper").  The N = frames * height *
+ * width video tokens form a latent grid in (frame, row, column) raster order
+ * and are cut into 3D tiles of (4, 4, 4) tokens, numbered in raster order over
+ * the tile grid; tiles on the far edges hold fewer tokens where a side is not
+ * a multiple of 4.  Per head:
+ *   1. coarse stage: score(b, c) = mean_{i in b} q_i . mean_{j in c} k_j for
+ *      every query tile b and key tile c (float32);
+ *   2. each query tile b keeps the topk key tiles with the highest scores,
+ *      ties to the lower tile index;
+ *   3. fine stage: o_i = softmax_j(scale q_i.k_j) v_j over the tokens j of the
+ *      tiles b kept, for every token i of b (float32 softmax, bf16 P.V).
+ * The page's count of kept tiles is fv_vsa_topk(num_tiles, sparsity).  The
+ * learned compression branch is not part of this call (its gate needs
+ * trained weights and starts at zero).
+ *
+ * Q, K, V, O:   device bf16 [N, H*128], as fv_attn_fwd.
+ * frames, height, width: the latent grid, each >= 4; N must equal their
+ *               product; at most 16,384 tiles.
+ * topk:         1 .. fv_vsa_num_tiles(frames, height, width).
+ * selected:     device int32 [H, num_tiles, topk], written: the kept tiles of
+ *               every query tile, ascending.
+ * workspace:    device scratch of at least fv_vsa_workspace_bytes(...) bytes
+ *               (256-byte aligned), caller-owned; workspace_bytes is its size.
+ * lse:          nullable device float32 [H, N], as fv_attn_fwd.
+ * Errors: FV_ERR_NULL, FV_ERR_SHAPE (grid, N, topk, tile count, D, H),
+ * FV_ERR_ALIGN (16-byte Q/K/V/O, 4-byte selected and lse, 256-byte
+ * workspace), FV_ERR_ARG (scale not finite and > 0, workspace too small),
+ * FV_ERR_ALIAS (O or selected or workspace overlapping another buffer).
+ * All heads run in one launch sequence on `stream`.
+ */
+fv_status fv_vsa_attn(const void *Q, const void *K, const void *V, void *O, int64_t N, int H, int D,
+                      float scale, int frames, int height, int width, int topk, int32_t *selected,
+                      void *workspace, int64_t workspace_bytes, float *lse, void *stream);
+
+/* Number of (4, 4, 4) tiles of the grid; 0 for a side < 1, -1 above 16,384. */
+int fv_vsa_num_tiles(int frames, int height, int width);
+
+/* The page's count of kept tiles, max(1, min(ceil((1 - sparsity) * num_tiles),
+ * num_tiles)), evaluated in double; 0 when num_tiles < 1 or sparsity is NaN. */
+int fv_vsa_topk(int num_tiles, double sparsity);
+
+/* Scratch bytes fv_vsa_attn needs for H heads, the grid and topk; -1 on bad sizes. */
+int64_t fv_vsa_workspace_bytes(int H, int frames, int height, int width, int topk);
+
+/*
  * Cached-AdaLN modulated LayerNorm of the residual stream for one schedule step:
  *   mu = mean_c x[i,c],  var = mean_c (x[i,c] - mu)^2   (biased)
  *   y[i,c] = (x[i,c] - mu) / sqrt(var + eps) * (1 + scale_table[step*ld + c])

@@ -97,6 +97,18 @@ def fine_rows(q, k, v, rows, row_tile, selected, tiles, scale: float) -> np.ndar
     return out
 
 
+def fine_lse(q, k, rows, row_tile, selected, tiles, scale: float) -> np.ndarray:
+    """float64 log-sum-exp of each query row's scores over its kept keys."""
+    q64, k64 = np.asarray(q, dtype=np.float64), np.asarray(k, dtype=np.float64)
+    out = np.empty(len(rows))
+    for r, i in enumerate(rows):
+        keys = np.concatenate([tiles[c] for c in selected[row_tile[i]]])
+        s = scale * (k64[keys] @ q64[i])
+        m = s.max()
+        out[r] = m + np.log(np.exp(s - m).sum())
+    return out
+
+
 def token_tile(frames: int, height: int, width: int) -> np.ndarray:
     """Tile index of every token ([N])."""
     tiles = tile_tokens(frames, height, width)

@@ -153,3 +153,33 @@ def test_tagged_ops_reject_bad_arguments(lib):
     assert lib.fv_gated_residual_tagged(A, B, O, 5040, 5376, C, 5376, 8, 3, 3, None, None) == -1
     assert lib.fv_gated_residual_tagged(A, B, O, 5040, 5376, C, 5376, 8, 3, -1, T, None) == -4
     assert lib.fv_gated_residual_tagged(A, B, B, 5040, 5376, C, 5376, 8, 3, 3, T, None) == -9
+
+
+def vsa(lib, q=A, k=B, v=C, o=O, n=4 * 8 * 12, h=2, d=128, scale=0.088, f=4, hh=8, w=12, topk=2, sel=T,
+        ws=T + (1 << 30), wsb=1 << 30, lse=None):
+    return lib.fv_vsa_attn(q, k, v, o, n, h, d, scale, f, hh, w, topk, sel, ws, wsb, lse, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(sel=None), -1), (dict(ws=None), -1),
+    (dict(d=64), -2), (dict(f=3), -2), (dict(w=2), -2), (dict(n=4 * 8 * 12 - 1), -2), (dict(topk=0), -2),
+    (dict(topk=7), -2), (dict(h=0), -2), (dict(f=4, hh=4, w=4 * 16385, n=4 * 4 * 4 * 16385), -2),
+    (dict(scale=0.0), -8), (dict(scale=float("nan")), -8), (dict(wsb=64), -8),
+    (dict(q=A + 8), -3), (dict(ws=T + (1 << 30) + 16), -3), (dict(sel=T + 2), -3),
+    (dict(o=A), -9), (dict(sel=A + 64), -9), (dict(sel=T + 224, ws=T + 256), -9), (dict(lse=O + 1024), -9),
+])
+def test_vsa_rejects_bad_arguments(lib, kw, code):
+    assert vsa(lib, **kw) == code
+
+
+def test_vsa_host_helpers_follow_the_printed_count(lib):
+    from oracle import vsa as VS
+    for grid in [(72, 24, 42), (5, 6, 7), (4, 4, 4), (102, 24, 42)]:
+        assert fv.vsa_num_tiles(*grid) == len(VS.tile_tokens(*grid))
+    assert fv.vsa_num_tiles(0, 4, 4) == 0 and fv.vsa_num_tiles(4, 4, 4 * 16385) == -1
+    for n in (1, 2, 7, 64, 594, 1188, 1716):
+        for s in (0.0, 0.5, 0.75, 0.9, 0.95, 1.0, -0.5, 1.5):
+            assert fv.vsa_topk(n, s) == VS.topk_count(n, s), (n, s)
+    assert fv.vsa_topk(0, 0.9) == 0 and fv.vsa_topk(10, float("nan")) == 0
+    assert lib.fv_vsa_workspace_bytes(2, 4, 8, 12, 2) > 0
+    assert lib.fv_vsa_workspace_bytes(2, 4, 8, 12, 7) == -1

@@ -82,8 +82,12 @@ def test_zero_sparsity_is_dense_attention():
         sl = slice(h * D, (h + 1) * D)
         got, sel = S.vsa_head(q[:, sl].double().numpy(), k[:, sl].double().numpy(), v[:, sl].double().numpy(),
                               rows, frames, height, width, S.topk_count(ntiles, 0.0), scale)
-        want, _ = oracle.attn_rows(q, k, v, h, rows, scale)
+        want, want_lse = oracle.attn_rows(q, k, v, h, rows, scale)
         assert np.abs(got - want).max() < 1e-12
+        tiles = S.tile_tokens(frames, height, width)
+        lse = S.fine_lse(q[:, sl].double().numpy(), k[:, sl].double().numpy(), rows,
+                         S.token_tile(frames, height, width), sel, tiles, scale)
+        assert np.abs(lse - want_lse).max() < 1e-12
         assert np.array_equal(sel, np.tile(np.arange(ntiles), (ntiles, 1)))
 
 
@@ -176,10 +180,12 @@ MUTANTS = {
     "grid_rounds_down": ("-(-width // TILE[2])", "(width // TILE[2])"),
     "height_width_swapped": ("(t * height + h) * width + w", "(t * width + w) * height + h"),
     "mean_over_full_tile": ("/ np.float32(len(idx))", "/ np.float32(64)"),
-    "scale_dropped": ("s = scale * (k64[keys] @ q64[i])", "s = (k64[keys] @ q64[i])"),
+    "scale_dropped": ("s = scale * (k64[keys] @ q64[i])\n        e = np.exp", "s = (k64[keys] @ q64[i])\n        e = np.exp"),
     "queries_pooled_from_keys": ("select(coarse_scores(pooled(q, tiles), pooled(k, tiles)), topk)",
                                  "select(coarse_scores(pooled(k, tiles), pooled(k, tiles)), topk)"),
-    "row_tile_from_key_side": ("for c in selected[row_tile[i]]", "for c in selected[min(row_tile[i] + 1, len(selected) - 1)]"),
+    "row_tile_off_by_one": ("for c in selected[row_tile[i]]])\n        s = scale * (k64[keys] @ q64[i])\n        e =",
+                            "for c in selected[min(row_tile[i] + 1, len(selected) - 1)]])\n"
+                            "        s = scale * (k64[keys] @ q64[i])\n        e ="),
 }
 
 

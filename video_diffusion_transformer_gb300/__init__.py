@@ -25,7 +25,8 @@ STATUS = {
 # every symbol include/fv.h declares
 EXPORTS = ("fv_attn_fwd", "fv_adaln_modulate", "fv_gated_residual", "fv_step_for_timestep", "fv_sync_status",
            "fv_status_string", "fv_version", "fv_attn_fwd_noalloc", "fv_attn_fwd_window",
-           "fv_adaln_modulate_tagged", "fv_gated_residual_tagged", "fv_delta_attn")
+           "fv_adaln_modulate_tagged", "fv_gated_residual_tagged", "fv_delta_attn", "fv_vsa_attn",
+           "fv_vsa_num_tiles", "fv_vsa_topk", "fv_vsa_workspace_bytes")
 NOALLOC_MAX_LAUNCHES = 64
 
 HEAD_DIM = 128
@@ -58,6 +59,14 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fv_attn_fwd_window.restype = i32
     lib.fv_delta_attn.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, vp, vp, vp, vp]
     lib.fv_delta_attn.restype = i32
+    lib.fv_vsa_attn.argtypes = [vp, vp, vp, vp, i64, i32, i32, f32, i32, i32, i32, i32, vp, vp, i64, vp, vp]
+    lib.fv_vsa_attn.restype = i32
+    lib.fv_vsa_num_tiles.argtypes = [i32, i32, i32]
+    lib.fv_vsa_num_tiles.restype = i32
+    lib.fv_vsa_topk.argtypes = [i32, ctypes.c_double]
+    lib.fv_vsa_topk.restype = i32
+    lib.fv_vsa_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    lib.fv_vsa_workspace_bytes.restype = i64
     lib.fv_adaln_modulate.argtypes = [vp, vp, i32, i64, i32, vp, vp, i64, i32, i32, f32, vp]
     lib.fv_adaln_modulate.restype = i32
     lib.fv_gated_residual.argtypes = [vp, vp, vp, i64, i32, vp, i64, i32, i32, vp]
@@ -200,6 +209,64 @@ def delta_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Te
         _dev(states, "states", torch.float32), _dev(workspace, "workspace", torch.float32), _stream_ptr(stream))
     _check(code, "fv_delta_attn")
     return out, states
+
+
+def vsa_num_tiles(frames: int, height: int, width: int) -> int:
+    """Tiles of the (4, 4, 4) tiling of a latent grid (fv_vsa_num_tiles)."""
+    return int(load_library().fv_vsa_num_tiles(int(frames), int(height), int(width)))
+
+
+def vsa_topk(num_tiles: int, sparsity: float) -> int:
+    """Kept key tiles per query tile for a sparsity (fv_vsa_topk)."""
+    return int(load_library().fv_vsa_topk(int(num_tiles), float(sparsity)))
+
+
+def vsa_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, frames: int, height: int, width: int,
+             topk: int | None = None, sparsity: float = 0.9, scale: float = DEFAULT_SCALE,
+             out: torch.Tensor | None = None, selected: torch.Tensor | None = None,
+             workspace: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """VSA-style block-sparse attention over a (frames, height, width) latent grid.
+
+    q, k, v: bf16 [N, H*128] with N = frames*height*width in raster order.
+    ``topk`` (default: the count for ``sparsity``) key tiles are kept per
+    query tile.  Returns (O bf16 [N, H*128], selected int32 [H, tiles, topk]).
+    ``workspace`` (uint8, at least fv_vsa_workspace_bytes) avoids an
+    allocation per call.
+    """
+    lib = load_library()
+    n = q.shape[0]
+    width_all = q.numel() // max(1, n)
+    h = width_all // HEAD_DIM
+    if h * HEAD_DIM != width_all or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [N, H*128]")
+    nt = vsa_num_tiles(frames, height, width)
+    if nt < 1:
+        raise ValueError("bad latent grid")
+    if topk is None:
+        topk = vsa_topk(nt, sparsity)
+    if out is None:
+        out = torch.empty_like(q)
+    if selected is None:
+        selected = torch.empty((h, nt, topk), dtype=torch.int32, device=q.device)
+    if selected.shape != (h, nt, topk):
+        raise ValueError("selected must be int32 [H, tiles, topk]")
+    need = int(lib.fv_vsa_workspace_bytes(h, int(frames), int(height), int(width), int(topk)))
+    if need < 0:
+        raise FvError(-2, "fv_vsa_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    lse_ptr = None
+    if lse is not None:
+        if lse.shape != (h, n):
+            raise ValueError("lse must be float32 [H, N]")
+        lse_ptr = _dev(lse, "lse", torch.float32)
+    code = lib.fv_vsa_attn(_dev(q, "q", torch.bfloat16), _dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16),
+                           _dev(out, "out", torch.bfloat16), n, h, HEAD_DIM, float(scale), int(frames), int(height),
+                           int(width), int(topk), _dev(selected, "selected", torch.int32),
+                           _dev(workspace, "workspace", torch.uint8), workspace.numel(), lse_ptr,
+                           _stream_ptr(stream))
+    _check(code, "fv_vsa_attn")
+    return out, selected
 
 
 def attn_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor | None = None, *,

@@ -614,11 +614,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // -------------------------------------------------------------- host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// [n, ld] bf16 row-major, boxes of 128 rows x 64 columns, 128-byte swizzle,
+// zero fill outside the tensor.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t n, int ld) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)n};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2u};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)kRows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
-EncodeTiledFn encode_fn() {
+}  // namespace
+
+EncodeTiledFn tensor_map_encoder() {
     static EncodeTiledFn fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -631,22 +643,6 @@ EncodeTiledFn encode_fn() {
     });
     return fn;
 }
-
-// [n, ld] bf16 row-major, boxes of 128 rows x 64 columns, 128-byte swizzle,
-// zero fill outside the tensor.
-bool make_map(CUtensorMap *m, const void *ptr, int64_t n, int ld) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)n};
-    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2u};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)kRows};
-    const cuuint32_t estr[2] = {1u, 1u};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-}  // namespace
 
 fv_status launch_attn_fwd(const AttnLaunch &a, cudaStream_t stream) {
     static std::mutex mu;

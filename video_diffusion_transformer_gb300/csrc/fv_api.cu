@@ -163,6 +163,73 @@ fv_status fv_delta_attn(const void *Q, const void *K, const void *V, const float
     return fv::launch_delta_attn(a, static_cast<cudaStream_t>(stream));
 }
 
+int fv_vsa_num_tiles(int frames, int height, int width) { return fv::vsa_num_tiles(frames, height, width); }
+
+int fv_vsa_topk(int num_tiles, double sparsity) {
+    if (num_tiles < 1 || std::isnan(sparsity)) return 0;
+    const double want = std::ceil((1.0 - sparsity) * (double)num_tiles);
+    if (!(want < (double)num_tiles)) return num_tiles;  // also +inf
+    return want < 1.0 ? 1 : (int)want;
+}
+
+int64_t fv_vsa_workspace_bytes(int H, int frames, int height, int width, int topk) {
+    const int nt = fv::vsa_num_tiles(frames, height, width);
+    if (H < 1 || H > 256 || nt < 1 || topk < 1 || topk > nt) return -1;
+    return fv::vsa_workspace_bytes(H, frames, height, width, topk);
+}
+
+fv_status fv_vsa_attn(const void *Q, const void *K, const void *V, void *O, int64_t N, int H, int D, float scale,
+                      int frames, int height, int width, int topk, int32_t *selected, void *workspace,
+                      int64_t workspace_bytes, float *lse, void *stream) {
+    if (!Q || !K || !V || !O || !selected || !workspace) return FV_ERR_NULL;
+    if (D != 128 || H < 1 || H > 256 || frames < 4 || height < 4 || width < 4 || N < 1 ||
+        N >= (int64_t(1) << 31) || N != (int64_t)frames * height * width)
+        return FV_ERR_SHAPE;
+    const int nt = fv::vsa_num_tiles(frames, height, width);
+    if (nt < 1 || topk < 1 || topk > nt) return FV_ERR_SHAPE;
+    if (!std::isfinite(scale) || !(scale > 0.0f)) return FV_ERR_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(selected, 4) ||
+        !aligned(workspace, 256) || (lse && !aligned(lse, 4)))
+        return FV_ERR_ALIGN;
+    const int64_t need = fv::vsa_workspace_bytes(H, frames, height, width, topk);
+    if (workspace_bytes < need) return FV_ERR_ARG;
+    const size_t act = (size_t)N * (size_t)H * 128u * 2u;
+    const size_t selb = (size_t)H * (size_t)nt * (size_t)topk * 4u;
+    const size_t lseb = (size_t)H * (size_t)N * 4u;
+    const void *ins[3] = {Q, K, V};
+    for (const void *in : ins) {
+        if (overlaps(O, act, in, act) || overlaps(selected, selb, in, act) || overlaps(workspace, need, in, act) ||
+            (lse && overlaps(lse, lseb, in, act)))
+            return FV_ERR_ALIAS;
+    }
+    if (overlaps(O, act, selected, selb) || overlaps(O, act, workspace, need) ||
+        overlaps(selected, selb, workspace, need) ||
+        (lse && (overlaps(lse, lseb, O, act) || overlaps(lse, lseb, selected, selb) ||
+                 overlaps(lse, lseb, workspace, need))))
+        return FV_ERR_ALIAS;
+    DeviceState *d = nullptr;
+    fv_status st = device_state(&d);
+    if (st != FV_OK) return st;
+    fv::VsaLaunch a;
+    a.q = Q;
+    a.k = K;
+    a.v = V;
+    a.o = O;
+    a.lse = lse;
+    a.selected = selected;
+    a.n = N;
+    a.heads = H;
+    a.frames = frames;
+    a.height = height;
+    a.width = width;
+    a.topk = topk;
+    a.scale = scale;
+    a.workspace = workspace;
+    a.status = d->status;
+    a.num_sms = d->num_sms;
+    return fv::launch_vsa_attn(a, static_cast<cudaStream_t>(stream));
+}
+
 fv_status fv_adaln_modulate(const void *x, void *y, int y_is_fp32, int64_t N, int C, const float *shift_table,
                             const float *scale_table, int64_t table_ld, int num_steps, int step, float eps,
                             void *stream) {

@@ -1,6 +1,7 @@
 // Internal declarations shared by the C-ABI layer and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -13,6 +14,12 @@ namespace fv {
 constexpr int kDevTimeout = 0x7100;
 // A per-token modality tag was >= the number of modalities; the row was skipped.
 constexpr int kDevBadTag = 0x7200;
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (null if absent).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
 
 struct AttnLaunch {
     const void *q, *k, *v;
@@ -64,6 +71,28 @@ struct DeltaLaunch {
 
 // Enqueue the Video Delta Attention kernels (stats, solve, scan, readout).
 fv_status launch_delta_attn(const DeltaLaunch &a, cudaStream_t stream);
+
+struct VsaLaunch {
+    const void *q, *k, *v;        // bf16 [n, heads * 128], tokens in (frame, row, column) raster order
+    void *o;                      // bf16 [n, heads * 128]
+    float *lse;                   // [heads, n] or null
+    int32_t *selected;            // [heads, num_tiles, topk]
+    int64_t n;
+    int heads;
+    int frames, height, width;    // latent grid, n = frames * height * width
+    int topk;
+    float scale;
+    void *workspace;              // vsa_workspace_bytes(...) bytes
+    int *status;
+    int num_sms;
+};
+
+// Tiles of the (4, 4, 4) tiling of a latent grid.
+int vsa_num_tiles(int frames, int height, int width);
+// Bytes of scratch fv_vsa_attn needs (tile means, per-pair kept-tile lists).
+int64_t vsa_workspace_bytes(int heads, int frames, int height, int width, int topk);
+// Enqueue the VSA kernels (tile means, selection, block-sparse attention).
+fv_status launch_vsa_attn(const VsaLaunch &a, cudaStream_t stream);
 
 fv_status launch_adaln_modulate_tagged(const TaggedRows &t, const void *x, void *y, bool y_fp32, int64_t n, int c,
                                        float eps, int num_sms, cudaStream_t stream);

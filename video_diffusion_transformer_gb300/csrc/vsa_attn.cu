@@ -1,0 +1,815 @@
+// VSA-style block-sparse attention over a video latent grid for sm_103a.
+//
+// "FastH3 Preview v1: four calls, one-tenth the attention, and what the 14x
+// actually measures", section "Lever two: VSA-H3 makes each of the four calls
+// cheaper": the video tokens of a (frames, height, width) latent grid are cut
+// into 3D tiles of (4, 4, 4) = 64 tokens; a coarse stage scores every (query
+// tile, key tile) pair from the tiles' mean query and mean key; each query
+// tile keeps its top-k key tiles; every query then attends exactly, with the
+// softmax, to the keys of its tile's kept tiles.  Tiles on the far edges of
+// the grid hold fewer tokens; their means are over their own tokens and their
+// missing tokens are masked.  Ties in the coarse score go to the lower tile.
+//
+// Three kernels:
+//   vsa_pool    (tile): float32 means of q and k of every head over the tile;
+//   vsa_select  (head, pair of query tiles 2p, 2p+1): coarse scores against
+//               every key tile, the top-k of each of the two rows (a 32-step
+//               search for the k-th largest score, ties to the lower index),
+//               written as ascending tile lists, and the union of the two
+//               lists with one owner bit per query tile;
+//   vsa_fine    (persistent, one CTA per SM): unit = (head, pair).  A 128-row
+//               Q tile holds the pair's two query tiles (rows 0-63, 64-127),
+//               each brought in by one 4D TMA box {64 channels, 4, 4, 4}
+//               straight from the token-major tensor, so no permuted copy is
+//               made; a K/V tile holds two key tiles of the union.  A warp's
+//               32 rows all belong to one query tile, so which of the two key
+//               tiles it sees is one warp-uniform bit each.  The two softmax
+//               warpgroups split the K/V tiles of a unit (even / odd) and keep
+//               their own running max, sum and O in tensor memory; at the end
+//               of the unit they exchange (max, sum) through shared memory and
+//               each writes half of the merged output columns.
+// All waits are bounded; a wait that runs out records kDevTimeout | where.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "fv_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fv {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTok = 64;                      // tokens of a tile
+constexpr int kRows = 128;                    // rows of a Q tile, keys of a K/V tile
+constexpr int kStages = 4;                    // K/V ring slots
+constexpr int kHalfBytes = kRows * 64 * 2;    // 128 rows x 64 channels (16 KB)
+constexpr int kTileBytes = 2 * kHalfBytes;    // 32 KB
+constexpr int kBoxBytes = kTok * 64 * 2;      // one tile x 64 channels (8 KB)
+constexpr int kThreads = 320;                 // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr int kMaxTiles = 16384;              // tile index fits the low 16 bits of a list entry
+
+constexpr int kBarKvFull = 0;
+constexpr int kBarKvEmpty = kBarKvFull + kStages;
+constexpr int kBarQFull = kBarKvEmpty + kStages;
+constexpr int kBarQEmpty = kBarQFull + 2;
+constexpr int kBarSFull = kBarQEmpty + 2;
+constexpr int kBarPFull = kBarSFull + 2;
+constexpr int kBarOFull = kBarPFull + 2;
+constexpr int kBarMlReady = kBarOFull + 2;
+constexpr int kBarMerged = kBarMlReady + 1;
+constexpr int kBarDrain = kBarMerged + 1;
+constexpr int kNumBars = kBarDrain + 1;
+
+constexpr int kSmemQ = 0;
+constexpr int kSmemKV = kSmemQ + 2 * kTileBytes;
+constexpr int kSmemMl = kSmemKV + kStages * kTileBytes;   // [2 units][2 groups][max, sum][128] float
+constexpr int kSmemBar = kSmemMl + 2 * 2 * 2 * kRows * 4;
+constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
+constexpr int kSmemBytes = kSmemMisc + 16 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+constexpr int kWhereQEmpty = 1, kWhereKvEmpty = 2, kWhereQFull = 3, kWhereKvFull = 4, kWherePFull = 5,
+              kWhereSFull = 6, kWhereOFull = 7, kWhereDrain = 8, kWhereMl = 9, kWhereMerged = 10;
+
+struct Geo {
+    int frames, height, width;
+    int tiles_h, tiles_w;  // tile grid along h and w
+    int num_tiles;
+};
+
+struct TileCoord {
+    int t0, h0, w0;  // first token of the tile along each axis
+};
+
+__host__ __device__ __forceinline__ TileCoord tile_coord(const Geo &g, int tile) {
+    TileCoord c;
+    c.w0 = 4 * (tile % g.tiles_w);
+    c.h0 = 4 * ((tile / g.tiles_w) % g.tiles_h);
+    c.t0 = 4 * (tile / (g.tiles_w * g.tiles_h));
+    return c;
+}
+
+// Bit r of the result is set when row r = 16 lt + 4 lh + lw of the tile's
+// box is a token of the grid.
+__device__ __forceinline__ uint64_t tile_token_mask(const Geo &g, int tile) {
+    const TileCoord c = tile_coord(g, tile);
+    const int nw = min(4, g.width - c.w0), nh = min(4, g.height - c.h0), nt = min(4, g.frames - c.t0);
+    const uint32_t row = (1u << nw) - 1u;
+    uint32_t plane = 0;
+    for (int i = 0; i < nh; ++i) plane |= row << (4 * i);
+    uint64_t m = 0;
+    for (int i = 0; i < nt; ++i) m |= (uint64_t)plane << (16 * i);
+    return m;
+}
+
+// ----------------------------------------------------------------- pool
+// Means of q and k of every head over the tokens of tile blockIdx.x: thread
+// handles 8 channels (16 bytes) at a time, tokens in the tile's raster order.
+__global__ void __launch_bounds__(256)
+    vsa_pool_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k, Geo g, int heads,
+                    float *__restrict__ qbar, float *__restrict__ kbar) {
+    const int tile = (int)blockIdx.x;
+    const TileCoord c = tile_coord(g, tile);
+    const int nw = min(4, g.width - c.w0), nh = min(4, g.height - c.h0), nt = min(4, g.frames - c.t0);
+    const int ld = heads * kD;
+    const float count = (float)(nw * nh * nt);
+    for (int ch = (int)threadIdx.x; ch < ld / 8; ch += (int)blockDim.x) {
+        float sq[8], sk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sq[e] = sk[e] = 0.f;
+        for (int lt = 0; lt < nt; ++lt)
+            for (int lh = 0; lh < nh; ++lh)
+                for (int lw = 0; lw < nw; ++lw) {
+                    const int64_t tok = ((int64_t)(c.t0 + lt) * g.height + (c.h0 + lh)) * g.width + (c.w0 + lw);
+                    const uint4 a = *reinterpret_cast<const uint4 *>(q + tok * ld + ch * 8);
+                    const uint4 b = *reinterpret_cast<const uint4 *>(k + tok * ld + ch * 8);
+                    const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
+                    const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 fa = __bfloat1622float2(pa[e]), fb = __bfloat1622float2(pb[e]);
+                        sq[2 * e] += fa.x;
+                        sq[2 * e + 1] += fa.y;
+                        sk[2 * e] += fb.x;
+                        sk[2 * e + 1] += fb.y;
+                    }
+                }
+        const int h = (ch * 8) / kD, d = (ch * 8) % kD;
+        float *dq = qbar + ((size_t)h * g.num_tiles + tile) * kD + d;
+        float *dk = kbar + ((size_t)h * g.num_tiles + tile) * kD + d;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            dq[e] = sq[e] / count;
+            dk[e] = sk[e] / count;
+        }
+    }
+}
+
+// --------------------------------------------------------------- select
+// Order-preserving key of a float score (+0 and -0 map to the same key).
+__device__ __forceinline__ uint32_t score_key(float f) {
+    const uint32_t u = __float_as_uint(f + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The k-th largest key of keys[0, n), found bit by bit by one warp.
+__device__ uint32_t kth_largest_key(const uint32_t *keys, int n, int k, int lane) {
+    uint32_t t = 0;
+    for (int b = 31; b >= 0; --b) {
+        const uint32_t cand = t | (1u << b);
+        int cnt = 0;
+        for (int i = lane; i < n; i += 32) cnt += keys[i] >= cand ? 1 : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        if (cnt >= k) t = cand;
+    }
+    return t;
+}
+
+// One CTA per (pair p, head): scores of query tiles 2p and 2p+1 against every
+// key tile, their top-k lists and the union list.
+__global__ void __launch_bounds__(256)
+    vsa_select_kernel(const float *__restrict__ qbar, const float *__restrict__ kbar, Geo g, int pairs, int topk,
+                      int32_t *__restrict__ selected, int32_t *__restrict__ lists, int32_t *__restrict__ counts) {
+    extern __shared__ uint32_t keys[];  // [2][num_tiles]
+    __shared__ uint32_t thr[2];
+    const int p = (int)blockIdx.x, h = (int)blockIdx.y;
+    const int nt = g.num_tiles;
+    const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
+    const int r1 = 2 * p + 1 < nt ? 2 * p + 1 : 2 * p;  // a lone last tile scores twice, kept once
+    const float4 qa = reinterpret_cast<const float4 *>(qbar + ((size_t)h * nt + 2 * p) * kD)[lane];
+    const float4 qb = reinterpret_cast<const float4 *>(qbar + ((size_t)h * nt + r1) * kD)[lane];
+    for (int c = warp; c < nt; c += 8) {
+        const float4 kk = reinterpret_cast<const float4 *>(kbar + ((size_t)h * nt + c) * kD)[lane];
+        float sa = qa.x * kk.x + qa.y * kk.y + qa.z * kk.z + qa.w * kk.w;
+        float sb = qb.x * kk.x + qb.y * kk.y + qb.z * kk.z + qb.w * kk.w;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sa += __shfl_xor_sync(0xffffffffu, sa, o);
+            sb += __shfl_xor_sync(0xffffffffu, sb, o);
+        }
+        if (lane == 0) {
+            keys[c] = score_key(sa);
+            keys[nt + c] = score_key(sb);
+        }
+    }
+    __syncthreads();
+    if (warp < 2) {
+        const uint32_t t = kth_largest_key(keys + warp * nt, nt, topk, lane);
+        if (lane == 0) thr[warp] = t;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    // One warp walks the tiles in ascending order, 32 at a time: a tile is kept
+    // when its key beats the threshold, or equals it and enough lower tiles
+    // with the same key have not already filled the k slots.
+    const bool has_b = 2 * p + 1 < nt;
+    const uint32_t ta = thr[0], tb = thr[1];
+    int gt_a = 0, gt_b = 0;
+    for (int i = lane; i < nt; i += 32) {
+        gt_a += keys[i] > ta ? 1 : 0;
+        gt_b += keys[nt + i] > tb ? 1 : 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        gt_a += __shfl_xor_sync(0xffffffffu, gt_a, o);
+        gt_b += __shfl_xor_sync(0xffffffffu, gt_b, o);
+    }
+    const int eq_room_a = topk - gt_a, eq_room_b = topk - gt_b;
+    int eq_a = 0, eq_b = 0, na = 0, nb = 0, nu = 0;
+    int32_t *sel_a = selected + ((size_t)h * nt + 2 * p) * topk;
+    int32_t *sel_b = selected + ((size_t)h * nt + 2 * p + 1) * topk;
+    int32_t *uni = lists + ((size_t)h * pairs + p) * 2 * topk;
+    const uint32_t below = (1u << lane) - 1u;
+    for (int base = 0; base < nt; base += 32) {
+        const int c = base + lane;
+        const bool in = c < nt;
+        const uint32_t ka = in ? keys[c] : 0u, kb = in ? keys[nt + c] : 0u;
+        const uint32_t ea = __ballot_sync(0xffffffffu, in && ka == ta);
+        const uint32_t eb = __ballot_sync(0xffffffffu, in && kb == tb);
+        const bool keep_a = in && (ka > ta || (ka == ta && eq_a + __popc(ea & below) < eq_room_a));
+        const bool keep_b = has_b && in && (kb > tb || (kb == tb && eq_b + __popc(eb & below) < eq_room_b));
+        const uint32_t ba = __ballot_sync(0xffffffffu, keep_a);
+        const uint32_t bb = __ballot_sync(0xffffffffu, keep_b);
+        const uint32_t bu = ba | bb;
+        if (keep_a) sel_a[na + __popc(ba & below)] = c;
+        if (keep_b) sel_b[nb + __popc(bb & below)] = c;
+        if (keep_a || keep_b)
+            uni[nu + __popc(bu & below)] = c | (keep_a ? 1 << 16 : 0) | (keep_b ? 1 << 17 : 0);
+        eq_a += __popc(ea);
+        eq_b += __popc(eb);
+        na += __popc(ba);
+        nb += __popc(bb);
+        nu += __popc(bu);
+    }
+    if (lane == 0) counts[(size_t)h * pairs + p] = nu;
+}
+
+// ----------------------------------------------------------------- fine
+struct Params {
+    __nv_bfloat16 *o;
+    float *lse;
+    int *status;
+    const int32_t *lists;   // [heads, pairs, 2 topk] union entries: tile | owner bits << 16
+    const int32_t *counts;  // [heads, pairs]
+    Geo g;
+    int n, ld, pairs, num_units, topk;
+    float scale_log2;
+};
+
+struct Smem {
+    uint32_t q, kv, bar;
+    float *ml;
+    volatile int *abort_flag;
+    __device__ uint32_t b(int i) const { return bar + 8u * (uint32_t)i; }
+};
+
+__device__ __forceinline__ bool wait_bar(const Smem &sm, int i, uint32_t parity, const Params &p, int where) {
+    return ptx::mbar_wait(sm.b(i), parity, sm.abort_flag, p.status, kDevTimeout | where);
+}
+
+__device__ __forceinline__ void drain_bar(const Smem &sm, int i, uint32_t parity, const Params &p) {
+    int never = 0;
+    ptx::mbar_wait(sm.b(i), parity, &never, p.status, kDevTimeout | kWhereDrain);
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1, int c2,
+                                            int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+        "[%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// Both channel halves of one tile into rows [64 half, 64 half + 64) of a
+// 32 KB operand tile.  A tile index past the grid loads a box that lies wholly
+// outside the tensor, which TMA fills with zeros.
+__device__ __forceinline__ void load_tile(const CUtensorMap *map, const Params &p, uint32_t dst, int half, int tile,
+                                          int x0, uint32_t bar) {
+    TileCoord c{p.g.frames, 0, 0};
+    if (tile < p.g.num_tiles) c = tile_coord(p.g, tile);
+    const uint32_t d = dst + (uint32_t)(half * kBoxBytes);
+    tma_load_4d(d, map, bar, x0, c.w0, c.h0, c.t0);
+    tma_load_4d(d + kHalfBytes, map, bar, x0 + 64, c.w0, c.h0, c.t0);
+}
+
+__device__ __forceinline__ int entry(const int32_t *lst, int count, int i) { return i < count ? lst[i] : 0xFFFF; }
+
+__device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv, const Params &p,
+                         const Smem &sm) {
+    uint32_t loads = 0;    // K/V tiles issued
+    uint32_t q_loads = 0;  // Q tiles issued (slot = count & 1)
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
+        const int head = unit / p.pairs, pr = unit % p.pairs;
+        const int x0 = head * kD;
+        const uint32_t qs = q_loads & 1u;
+        ok = wait_bar(sm, kBarQEmpty + (int)qs, ((q_loads >> 1) & 1u) ^ 1u, p, kWhereQEmpty);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(sm.b(kBarQFull + (int)qs), kTileBytes);
+        const uint32_t qdst = sm.q + qs * (uint32_t)kTileBytes;
+        load_tile(tq, p, qdst, 0, 2 * pr, x0, sm.b(kBarQFull + (int)qs));
+        load_tile(tq, p, qdst, 1, 2 * pr + 1, x0, sm.b(kBarQFull + (int)qs));
+        ++q_loads;
+        const int32_t *lst = p.lists + ((size_t)head * p.pairs + pr) * 2 * p.topk;
+        const int cnt = p.counts[(size_t)head * p.pairs + pr];
+        const int nkv = (cnt + 1) / 2;
+        auto load_kv = [&](const CUtensorMap *m, int j) -> bool {
+            const uint32_t s = loads % kStages, ph = (loads / kStages) & 1u;
+            if (!wait_bar(sm, kBarKvEmpty + (int)s, ph ^ 1u, p, kWhereKvEmpty)) return false;
+            ptx::mbar_arrive_expect_tx(sm.b(kBarKvFull + (int)s), kTileBytes);
+            const uint32_t dst = sm.kv + s * (uint32_t)kTileBytes;
+            load_tile(m, p, dst, 0, entry(lst, cnt, 2 * j) & 0xFFFF, x0, sm.b(kBarKvFull + (int)s));
+            load_tile(m, p, dst, 1, entry(lst, cnt, 2 * j + 1) & 0xFFFF, x0, sm.b(kBarKvFull + (int)s));
+            ++loads;
+            return true;
+        };
+        // the order the MMA warp consumes them: K0, K1, then V_j, K_{j+2}
+        ok = load_kv(tk, 0);
+        if (ok && nkv > 1) ok = load_kv(tk, 1);
+        for (int j = 0; ok && j < nkv; ++j) {
+            ok = load_kv(tv, j);
+            if (ok && j + 2 < nkv) ok = load_kv(tk, j + 2);
+        }
+    }
+    for (uint32_t s = 0; s < (uint32_t)kStages && s < loads; ++s) {
+        const uint32_t last = ((loads - 1u - s) / kStages) * kStages + s;
+        drain_bar(sm, kBarKvFull + (int)s, (last / kStages) & 1u, p);
+    }
+    for (uint32_t i = 0; i < 2u && i < q_loads; ++i) {
+        const uint32_t last = q_loads - 1u - i;  // the last Q load of each slot
+        drain_bar(sm, kBarQFull + (int)(last & 1u), (last >> 1) & 1u, p);
+    }
+}
+
+constexpr uint64_t kDescTile = (uint64_t)(kTileBytes >> 4);
+
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint64_t off = (uint64_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+        ptx::mma_ss(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc, bool accumulate) {
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, true);
+#pragma unroll
+    for (int kk = 0; kk < kRows / 16; ++kk) {
+        const uint64_t off = (uint64_t)((kk * 16 * 128) >> 4);
+        ptx::mma_ts(d_tmem, p_tmem + (uint32_t)(kk * 8), v_desc + off, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+__device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
+    const uint64_t q0 = ptx::sdesc_sw128(sm.q, 16, 1024);
+    const uint64_t kv0 = ptx::sdesc_sw128(sm.kv, 16, 1024);
+    const uint64_t v0 = ptx::sdesc_sw128(sm.kv, kHalfBytes, 1024);
+    uint32_t idx = 0, uu = 0, ptile[2] = {0u, 0u};
+    bool ok = true;
+    auto next_kv = [&](uint32_t &slot) -> bool {
+        slot = idx % kStages;
+        const bool r = wait_bar(sm, kBarKvFull + (int)slot, (idx / kStages) & 1u, p, kWhereKvFull);
+        ++idx;
+        if (r) ptx::tc_fence_after();
+        return r;
+    };
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x, ++uu) {
+        const int head = unit / p.pairs, pr = unit % p.pairs;
+        const uint32_t qs = uu & 1u;
+        ok = wait_bar(sm, kBarQFull + (int)qs, (uu >> 1) & 1u, p, kWhereQFull);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint64_t qd = q0 + qs * kDescTile;
+        const int nkv = (p.counts[(size_t)head * p.pairs + pr] + 1) / 2;
+        uint32_t s;
+        ok = next_kv(s);
+        if (!ok) break;
+        issue_qk(tmem, qd, kv0 + s * kDescTile);
+        ptx::tc_commit(sm.b(kBarSFull));
+        ptx::tc_commit(sm.b(kBarKvEmpty + (int)s));
+        if (nkv > 1) {
+            ok = next_kv(s);
+            if (!ok) break;
+            issue_qk(tmem + 128u, qd, kv0 + s * kDescTile);
+            ptx::tc_commit(sm.b(kBarSFull + 1));
+            ptx::tc_commit(sm.b(kBarKvEmpty + (int)s));
+        }
+        // both groups must have read O_0 and O_1 of the previous unit
+        if (uu > 0) {
+            ok = wait_bar(sm, kBarMerged, (uu - 1u) & 1u, p, kWhereMerged);
+            if (!ok) break;
+            ptx::tc_fence_after();
+        }
+        for (int j = 0; ok && j < nkv; ++j) {
+            const int k = j & 1;
+            ok = next_kv(s);
+            if (!ok) break;
+            ok = wait_bar(sm, kBarPFull + k, ptile[k] & 1u, p, kWherePFull);
+            if (!ok) break;
+            ++ptile[k];
+            ptx::tc_fence_after();
+            issue_pv(tmem + 256u + 128u * (uint32_t)k, tmem + 128u * (uint32_t)k, v0 + s * kDescTile, j >= 2);
+            ptx::tc_commit(sm.b(kBarKvEmpty + (int)s));
+            if (j + 2 >= nkv) ptx::tc_commit(sm.b(kBarOFull + k));
+            if (j + 2 < nkv) {
+                ok = next_kv(s);
+                if (!ok) break;
+                issue_qk(tmem + 128u * (uint32_t)k, qd, kv0 + s * kDescTile);
+                ptx::tc_commit(sm.b(kBarSFull + k));
+                ptx::tc_commit(sm.b(kBarKvEmpty + (int)s));
+            }
+        }
+        if (!ok) break;
+        if (nkv == 1) ptx::tc_commit(sm.b(kBarOFull + 1));  // group 1 had no tile
+        ptx::tc_commit(sm.b(kBarQEmpty + (int)qs));
+    }
+    ptx::tc_commit(sm.b(kBarDrain));
+    drain_bar(sm, kBarDrain, 0u, p);
+}
+
+// -------------------------------------------------------------- softmax
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Column c of a K/V tile is visible to the warp when bit (c % 32) of
+// mk[c / 32] is set.  Chunks with mk == 0 are skipped; kMasked tests single
+// columns (only edge tiles with missing tokens need it).
+template <bool kMasked>
+__device__ __forceinline__ float row_max(const uint32_t (&s)[4][32], const uint32_t (&mk)[4]) {
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+        if (mk[c4] == 0u) continue;
+        if (!kMasked) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                m0 = ptx::max3(m0, u2f(s[c4][i]), u2f(s[c4][i + 1]));
+                m1 = ptx::max3(m1, u2f(s[c4][i + 2]), u2f(s[c4][i + 3]));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if ((mk[c4] >> i) & 1u) m0 = fmaxf(m0, u2f(s[c4][i]));
+        }
+    }
+    return fmaxf(m0, m1);
+}
+
+template <bool kMasked>
+__device__ __forceinline__ float write_probs(const uint32_t (&s)[4][32], const uint32_t (&mk)[4], float scale_log2,
+                                             float m, uint32_t t_s) {
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t pk[16];
+        if (mk[c4] == 0u) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = 0u;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                float x0, x1, x2, x3;
+                ptx::fma2(x0, x1, u2f(s[c4][i]), u2f(s[c4][i + 1]), scale_log2, -m);
+                ptx::fma2(x2, x3, u2f(s[c4][i + 2]), u2f(s[c4][i + 3]), scale_log2, -m);
+                float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
+                float p2 = ptx::ex2_approx(x2), p3 = ptx::ex2_approx(x3);
+                if (kMasked) {
+                    p0 = ((mk[c4] >> i) & 1u) ? p0 : 0.f;
+                    p1 = ((mk[c4] >> (i + 1)) & 1u) ? p1 : 0.f;
+                    p2 = ((mk[c4] >> (i + 2)) & 1u) ? p2 : 0.f;
+                    p3 = ((mk[c4] >> (i + 3)) & 1u) ? p3 : 0.f;
+                }
+                ptx::add2(a0, a1, p0, p1);
+                ptx::add2(b0, b1, p2, p3);
+                pk[i / 2] = pack_bf16x2(p0, p1);
+                pk[i / 2 + 1] = pack_bf16x2(p2, p3);
+            }
+        }
+        ptx::tmem_st_32x32b_x16(t_s + (uint32_t)(c4 * 16), pk);
+    }
+    return (a0 + a1) + (b0 + b1);
+}
+
+// Softmax warpgroup k (0 or 1); thread t owns row t of the Q tile.
+__device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int k, int t) {
+    const uint32_t lane_base = (uint32_t)((t >> 5) * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + 128u * (uint32_t)k;
+    const uint32_t t_ok = tmem + lane_base + 256u + 128u * (uint32_t)k;
+    const int qhalf = t >> 6;   // which query tile of the pair this row belongs to
+    uint32_t seen = 0, uu = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x, ++uu) {
+        const int head = unit / p.pairs, pr = unit % p.pairs;
+        const int32_t *lst = p.lists + ((size_t)head * p.pairs + pr) * 2 * p.topk;
+        const int cnt = p.counts[(size_t)head * p.pairs + pr];
+        const int nkv = (cnt + 1) / 2;
+        float m_used = -INFINITY, l = 0.f;
+        for (int j = k; j < nkv; j += 2) {
+            ok = __all_sync(0xffffffffu, wait_bar(sm, kBarSFull + k, seen & 1u, p, kWhereSFull));
+            if (!ok) break;
+            ++seen;
+            ptx::tc_fence_after();
+            const int e0 = entry(lst, cnt, 2 * j), e1 = entry(lst, cnt, 2 * j + 1);
+            const uint64_t v0 = ((e0 >> (16 + qhalf)) & 1) ? tile_token_mask(p.g, e0 & 0xFFFF) : 0ull;
+            const uint64_t v1 = (2 * j + 1 < cnt && ((e1 >> (16 + qhalf)) & 1)) ? tile_token_mask(p.g, e1 & 0xFFFF)
+                                                                                : 0ull;
+            const uint32_t mk[4] = {(uint32_t)v0, (uint32_t)(v0 >> 32), (uint32_t)v1, (uint32_t)(v1 >> 32)};
+            if ((mk[0] | mk[1] | mk[2] | mk[3]) == 0u) {
+                uint32_t zero[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) zero[i] = 0u;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) ptx::tmem_st_32x32b_x16(t_s + (uint32_t)(c4 * 16), zero);
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(sm.b(kBarPFull + k));
+                continue;
+            }
+            uint32_t s[4][32];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) ptx::tmem_ld_32x32b_x32(t_s + (uint32_t)(32 * c4), s[c4]);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) ptx::reg_fence(s[c4]);
+            bool partial = false;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) partial |= mk[c4] != 0u && mk[c4] != 0xFFFFFFFFu;
+            const float m_tile = (partial ? row_max<true>(s, mk) : row_max<false>(s, mk)) * p.scale_log2;
+            float factor = 1.f;
+            bool rescale = false;
+            if (m_tile > m_used + kRescaleThreshold) {
+                if (m_used != -INFINITY) {
+                    factor = ptx::ex2_approx(m_used - m_tile);
+                    rescale = true;
+                }
+                m_used = m_tile;
+            }
+            const float tile_sum = partial ? write_probs<true>(s, mk, p.scale_log2, m_used, t_s)
+                                           : write_probs<false>(s, mk, p.scale_log2, m_used, t_s);
+            l = l * factor + tile_sum;
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t o[32];
+                    ptx::tmem_ld_32x32b_x32(t_ok + (uint32_t)(32 * c4), o);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence(o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * factor);
+                    ptx::tmem_st_32x32b_x32(t_ok + (uint32_t)(32 * c4), o);
+                }
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(sm.b(kBarPFull + k));
+        }
+        if (!ok) break;
+        ok = __all_sync(0xffffffffu, wait_bar(sm, kBarOFull + k, uu & 1u, p, kWhereOFull));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        // exchange the running max and sum with the other group
+        float *ml = sm.ml + (uu & 1u) * 4 * kRows;
+        ml[k * 2 * kRows + t] = m_used;
+        ml[k * 2 * kRows + kRows + t] = l;
+        ptx::mbar_arrive(sm.b(kBarMlReady));
+        ok = __all_sync(0xffffffffu, wait_bar(sm, kBarMlReady, uu & 1u, p, kWhereMl));
+        if (!ok) break;
+        const float m0 = ml[t], l0 = ml[kRows + t];
+        const float m1 = ml[2 * kRows + t], l1 = ml[3 * kRows + t];
+        const float mx = fmaxf(m0, m1);
+        const float a0 = l0 > 0.f ? ptx::ex2_approx(m0 - mx) : 0.f;
+        const float a1 = l1 > 0.f ? ptx::ex2_approx(m1 - mx) : 0.f;
+        const float sum = a0 * l0 + a1 * l1;
+        const float inv = 1.0f / sum;
+        // the row's token
+        const int tile = 2 * pr + qhalf, r = t & 63;
+        bool row_ok = tile < p.g.num_tiles;
+        int64_t tok = 0;
+        if (row_ok) {
+            const TileCoord c = tile_coord(p.g, tile);
+            const int tt = c.t0 + (r >> 4), hh = c.h0 + ((r >> 2) & 3), ww = c.w0 + (r & 3);
+            row_ok = tt < p.g.frames && hh < p.g.height && ww < p.g.width;
+            tok = ((int64_t)tt * p.g.height + hh) * p.g.width + ww;
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)tok * (size_t)p.ld + (size_t)head * kD + 64 * k);
+        const uint32_t t_o0 = tmem + lane_base + 256u + 64u * (uint32_t)k;
+#pragma unroll 1
+        for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t x0[32], x1[32];
+            ptx::tmem_ld_32x32b_x32(t_o0 + (uint32_t)(32 * c2), x0);
+            ptx::tmem_ld_32x32b_x32(t_o0 + 128u + (uint32_t)(32 * c2), x1);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence(x0);
+            ptx::reg_fence(x1);
+            if (row_ok) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float y0 = l0 > 0.f ? a0 * u2f(x0[8 * v + e]) : 0.f;
+                        const float y1 = l1 > 0.f ? a1 * u2f(x1[8 * v + e]) : 0.f;
+                        f[e] = (y0 + y1) * inv;
+                    }
+                    uint4 w;
+                    w.x = pack_bf16x2(f[0], f[1]);
+                    w.y = pack_bf16x2(f[2], f[3]);
+                    w.z = pack_bf16x2(f[4], f[5]);
+                    w.w = pack_bf16x2(f[6], f[7]);
+                    dst[c2 * 4 + v] = w;
+                }
+            }
+        }
+        if (k == 0 && row_ok && p.lse != nullptr)
+            p.lse[(size_t)head * (size_t)p.n + (size_t)tok] = (mx + log2f(sum)) * 0.69314718055994531f;
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(sm.b(kBarMerged));
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    vsa_fine_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    Smem sm;
+    sm.q = base + kSmemQ;
+    sm.kv = base + kSmemKV;
+    sm.bar = base + kSmemBar;
+    sm.ml = reinterpret_cast<float *>(smem + kSmemMl);
+    sm.abort_flag = reinterpret_cast<volatile int *>(smem + kSmemMisc + 4);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + kSmemMisc);
+    const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(sm.b(kBarKvFull + s), 1);
+            ptx::mbar_init(sm.b(kBarKvEmpty + s), 1);
+        }
+        for (int k = 0; k < 2; ++k) {
+            ptx::mbar_init(sm.b(kBarQFull + k), 1);
+            ptx::mbar_init(sm.b(kBarQEmpty + k), 1);
+            ptx::mbar_init(sm.b(kBarSFull + k), 1);
+            ptx::mbar_init(sm.b(kBarPFull + k), 128);
+            ptx::mbar_init(sm.b(kBarOFull + k), 1);
+        }
+        ptx::mbar_init(sm.b(kBarMlReady), 256);
+        ptx::mbar_init(sm.b(kBarMerged), 256);
+        ptx::mbar_init(sm.b(kBarDrain), 1);
+        *sm.abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kTmaWarp && lane == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
+    if (warp == kTmaWarp) {
+        if (lane == 0) producer(&tm_q, &tm_k, &tm_v, p, sm);
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) mma_issuer(p, sm, tmem);
+    } else {
+        softmax_role(p, sm, tmem, warp >> 2, (int)threadIdx.x & 127);
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// [frames, height, width, heads * 128] bf16 viewed as a 4D tensor; boxes of
+// one tile x 64 channels, 128-byte swizzle, zero fill outside the grid.
+bool make_grid_map(CUtensorMap *m, const void *ptr, const Geo &g, int ld) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t row = (cuuint64_t)ld * 2u;
+    const cuuint64_t dims[4] = {(cuuint64_t)ld, (cuuint64_t)g.width, (cuuint64_t)g.height, (cuuint64_t)g.frames};
+    const cuuint64_t strides[3] = {row, row * (cuuint64_t)g.width, row * (cuuint64_t)g.width * (cuuint64_t)g.height};
+    const cuuint32_t box[4] = {64u, 4u, 4u, 4u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+Geo make_geo(int frames, int height, int width) {
+    Geo g;
+    g.frames = frames;
+    g.height = height;
+    g.width = width;
+    g.tiles_h = (height + 3) / 4;
+    g.tiles_w = (width + 3) / 4;
+    g.num_tiles = ((frames + 3) / 4) * g.tiles_h * g.tiles_w;
+    return g;
+}
+
+size_t align256(size_t x) { return (x + 255u) & ~(size_t)255u; }
+
+struct WsLayout {
+    size_t qbar, kbar, lists, counts, total;
+};
+
+WsLayout ws_layout(int heads, const Geo &g, int topk) {
+    const int pairs = (g.num_tiles + 1) / 2;
+    WsLayout w;
+    const size_t means = align256((size_t)heads * g.num_tiles * kD * sizeof(float));
+    w.qbar = 0;
+    w.kbar = means;
+    w.lists = 2 * means;
+    w.counts = w.lists + align256((size_t)heads * pairs * 2 * topk * sizeof(int32_t));
+    w.total = w.counts + align256((size_t)heads * pairs * sizeof(int32_t));
+    return w;
+}
+
+}  // namespace
+
+int vsa_num_tiles(int frames, int height, int width) {
+    if (frames < 1 || height < 1 || width < 1) return 0;
+    const int64_t n = (int64_t)((frames + 3) / 4) * ((height + 3) / 4) * ((width + 3) / 4);
+    return n > kMaxTiles ? -1 : (int)n;
+}
+
+int64_t vsa_workspace_bytes(int heads, int frames, int height, int width, int topk) {
+    return (int64_t)ws_layout(heads, make_geo(frames, height, width), topk).total;
+}
+
+fv_status launch_vsa_attn(const VsaLaunch &a, cudaStream_t stream) {
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FV_ERR_LAUNCH;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(vsa_fine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+                    cudaSuccess ||
+                cudaFuncSetAttribute(vsa_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     2 * kMaxTiles * 4) != cudaSuccess)
+                return FV_ERR_LAUNCH;
+            attr_set[dev] = true;
+        }
+    }
+    const Geo g = make_geo(a.frames, a.height, a.width);
+    const int ld = a.heads * kD;
+    const int pairs = (g.num_tiles + 1) / 2;
+    const WsLayout w = ws_layout(a.heads, g, a.topk);
+    uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+    float *qbar = reinterpret_cast<float *>(ws + w.qbar);
+    float *kbar = reinterpret_cast<float *>(ws + w.kbar);
+    int32_t *lists = reinterpret_cast<int32_t *>(ws + w.lists);
+    int32_t *counts = reinterpret_cast<int32_t *>(ws + w.counts);
+    CUtensorMap mq, mk, mv;
+    if (!make_grid_map(&mq, a.q, g, ld) || !make_grid_map(&mk, a.k, g, ld) || !make_grid_map(&mv, a.v, g, ld))
+        return FV_ERR_LAUNCH;
+    const auto *q = static_cast<const __nv_bfloat16 *>(a.q);
+    const auto *k = static_cast<const __nv_bfloat16 *>(a.k);
+    vsa_pool_kernel<<<g.num_tiles, 256, 0, stream>>>(q, k, g, a.heads, qbar, kbar);
+    vsa_select_kernel<<<dim3(pairs, a.heads), 256, (size_t)2 * g.num_tiles * 4, stream>>>(
+        qbar, kbar, g, pairs, a.topk, a.selected, lists, counts);
+    Params p;
+    p.o = static_cast<__nv_bfloat16 *>(a.o);
+    p.lse = a.lse;
+    p.status = a.status;
+    p.lists = lists;
+    p.counts = counts;
+    p.g = g;
+    p.n = (int)a.n;
+    p.ld = ld;
+    p.pairs = pairs;
+    p.num_units = a.heads * pairs;
+    p.topk = a.topk;
+    p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
+    const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
+    vsa_fine_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
+}
+
+}  // namespace fv
