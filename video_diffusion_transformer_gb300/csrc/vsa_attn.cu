@@ -45,7 +45,14 @@ namespace {
 constexpr int kD = 128;
 constexpr int kTok = 64;                      // tokens of a tile
 constexpr int kRows = 128;                    // rows of a Q tile, keys of a K/V tile
-constexpr int kStages = 4;                    // K/V ring slots
+#ifndef VSA_KV_STAGES
+#define VSA_KV_STAGES 4
+#endif
+#ifndef VSA_Q_SLOTS
+#define VSA_Q_SLOTS 2
+#endif
+constexpr int kStages = VSA_KV_STAGES;        // K/V ring slots
+constexpr int kQSlots = VSA_Q_SLOTS;          // Q tiles in flight
 constexpr int kHalfBytes = kRows * 64 * 2;    // 128 rows x 64 channels (16 KB)
 constexpr int kTileBytes = 2 * kHalfBytes;    // 32 KB
 constexpr int kBoxBytes = kTok * 64 * 2;      // one tile x 64 channels (8 KB)
@@ -58,8 +65,8 @@ constexpr int kMaxTiles = 16384;              // tile index fits the low 16 bits
 constexpr int kBarKvFull = 0;
 constexpr int kBarKvEmpty = kBarKvFull + kStages;
 constexpr int kBarQFull = kBarKvEmpty + kStages;
-constexpr int kBarQEmpty = kBarQFull + 2;
-constexpr int kBarSFull = kBarQEmpty + 2;
+constexpr int kBarQEmpty = kBarQFull + kQSlots;
+constexpr int kBarSFull = kBarQEmpty + kQSlots;
 constexpr int kBarPFull = kBarSFull + 2;
 constexpr int kBarOFull = kBarPFull + 2;
 constexpr int kBarMlReady = kBarOFull + 2;
@@ -68,7 +75,7 @@ constexpr int kBarDrain = kBarMerged + 1;
 constexpr int kNumBars = kBarDrain + 1;
 
 constexpr int kSmemQ = 0;
-constexpr int kSmemKV = kSmemQ + 2 * kTileBytes;
+constexpr int kSmemKV = kSmemQ + kQSlots * kTileBytes;
 constexpr int kSmemMl = kSmemKV + kStages * kTileBytes;   // [2 units][2 groups][max, sum][128] float
 constexpr int kSmemBar = kSmemMl + 2 * 2 * 2 * kRows * 4;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
@@ -257,10 +264,10 @@ struct Params {
     __nv_bfloat16 *o;
     float *lse;
     int *status;
-    const int32_t *lists;   // [heads, pairs, 2 topk] union entries: tile | owner bits << 16
+    const int32_t *lists;   // [heads, pairs, list_ld] union entries: tile | owner bits << 16
     const int32_t *counts;  // [heads, pairs]
     Geo g;
-    int n, ld, pairs, num_units, topk;
+    int n, ld, pairs, num_units, list_ld;
     float scale_log2;
 };
 
@@ -301,38 +308,88 @@ __device__ __forceinline__ void load_tile(const CUtensorMap *map, const Params &
     tma_load_4d(d + kHalfBytes, map, bar, x0 + 64, c.w0, c.h0, c.t0);
 }
 
-__device__ __forceinline__ int entry(const int32_t *lst, int count, int i) { return i < count ? lst[i] : 0xFFFF; }
+// A softmax warp's view of one unit's list: for batches of 32 entries, one
+// per lane, the 64-bit mask of the tile's columns this warp's query tile
+// (owner bit 16 + qhalf) sees; the batch after next is already in flight.
+// Read with shuffles, so the per-tile path has no global-memory load.  Every
+// lane calls tile() with the same, never decreasing, index; entries past the
+// count read as 0xFFFF (no tile, no owner).
+struct MaskWindow {
+    const int32_t *lst;
+    const Geo *g;
+    int cnt, lane, base, qhalf;
+    uint32_t m0lo, m0hi, m1lo, m1hi;
+    int raw2;
+    __device__ __forceinline__ int ld(int batch) const {
+        const int i = batch * 32 + lane;
+        return i < cnt ? lst[i] : 0xFFFF;
+    }
+    __device__ __forceinline__ void masks(int e, uint32_t &lo, uint32_t &hi) const {
+        const uint64_t m = ((e >> (16 + qhalf)) & 1) ? tile_token_mask(*g, e & 0xFFFF) : 0ull;
+        lo = (uint32_t)m;
+        hi = (uint32_t)(m >> 32);
+    }
+    __device__ __forceinline__ void init(const int32_t *l, int c, int ln, int qh, const Geo *geo) {
+        lst = l;
+        cnt = c;
+        lane = ln;
+        qhalf = qh;
+        g = geo;
+        base = 0;
+        const int r0 = ld(0), r1 = ld(1);
+        raw2 = ld(2);
+        masks(r0, m0lo, m0hi);
+        masks(r1, m1lo, m1hi);
+    }
+    // columns of K/V tile j: mk[0..1] from entry 2j, mk[2..3] from entry 2j+1
+    __device__ __forceinline__ void tile(int j, uint32_t (&mk)[4]) {
+        while (((2 * j) >> 5) - base >= 1) {
+            m0lo = m1lo;
+            m0hi = m1hi;
+            masks(raw2, m1lo, m1hi);
+            raw2 = ld(base + 3);
+            ++base;
+        }
+        // entry 2j is in batch base; entry 2j + 1 is too (2j is even)
+        const int src = (2 * j) & 31;
+        mk[0] = __shfl_sync(0xffffffffu, m0lo, src);
+        mk[1] = __shfl_sync(0xffffffffu, m0hi, src);
+        mk[2] = __shfl_sync(0xffffffffu, m0lo, src + 1);
+        mk[3] = __shfl_sync(0xffffffffu, m0hi, src + 1);
+    }
+};
 
+// One thread (lane 0 of the TMA warp) issues every copy.
 __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv, const Params &p,
-                         const Smem &sm) {
-    uint32_t loads = 0;    // K/V tiles issued
-    uint32_t q_loads = 0;  // Q tiles issued (slot = count & 1)
+                         const Smem &sm, int lane) {
+    if (lane != 0) return;
+    uint32_t loads = 0, q_loads = 0;
     bool ok = true;
     for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
         const int head = unit / p.pairs, pr = unit % p.pairs;
         const int x0 = head * kD;
-        const uint32_t qs = q_loads & 1u;
-        ok = wait_bar(sm, kBarQEmpty + (int)qs, ((q_loads >> 1) & 1u) ^ 1u, p, kWhereQEmpty);
+        const uint32_t qs = q_loads % kQSlots;
+        ok = wait_bar(sm, kBarQEmpty + (int)qs, ((q_loads / kQSlots) & 1u) ^ 1u, p, kWhereQEmpty);
         if (!ok) break;
         ptx::mbar_arrive_expect_tx(sm.b(kBarQFull + (int)qs), kTileBytes);
         const uint32_t qdst = sm.q + qs * (uint32_t)kTileBytes;
         load_tile(tq, p, qdst, 0, 2 * pr, x0, sm.b(kBarQFull + (int)qs));
         load_tile(tq, p, qdst, 1, 2 * pr + 1, x0, sm.b(kBarQFull + (int)qs));
         ++q_loads;
-        const int32_t *lst = p.lists + ((size_t)head * p.pairs + pr) * 2 * p.topk;
+        const int32_t *lst = p.lists + ((size_t)head * p.pairs + pr) * p.list_ld;
         const int cnt = p.counts[(size_t)head * p.pairs + pr];
         const int nkv = (cnt + 1) / 2;
         auto load_kv = [&](const CUtensorMap *m, int j) -> bool {
             const uint32_t s = loads % kStages, ph = (loads / kStages) & 1u;
             if (!wait_bar(sm, kBarKvEmpty + (int)s, ph ^ 1u, p, kWhereKvEmpty)) return false;
+            const int e0 = 2 * j < cnt ? lst[2 * j] : 0xFFFF, e1 = 2 * j + 1 < cnt ? lst[2 * j + 1] : 0xFFFF;
             ptx::mbar_arrive_expect_tx(sm.b(kBarKvFull + (int)s), kTileBytes);
             const uint32_t dst = sm.kv + s * (uint32_t)kTileBytes;
-            load_tile(m, p, dst, 0, entry(lst, cnt, 2 * j) & 0xFFFF, x0, sm.b(kBarKvFull + (int)s));
-            load_tile(m, p, dst, 1, entry(lst, cnt, 2 * j + 1) & 0xFFFF, x0, sm.b(kBarKvFull + (int)s));
+            load_tile(m, p, dst, 0, e0 & 0xFFFF, x0, sm.b(kBarKvFull + (int)s));
+            load_tile(m, p, dst, 1, e1 & 0xFFFF, x0, sm.b(kBarKvFull + (int)s));
             ++loads;
             return true;
         };
-        // the order the MMA warp consumes them: K0, K1, then V_j, K_{j+2}
         ok = load_kv(tk, 0);
         if (ok && nkv > 1) ok = load_kv(tk, 1);
         for (int j = 0; ok && j < nkv; ++j) {
@@ -344,9 +401,9 @@ __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUt
         const uint32_t last = ((loads - 1u - s) / kStages) * kStages + s;
         drain_bar(sm, kBarKvFull + (int)s, (last / kStages) & 1u, p);
     }
-    for (uint32_t i = 0; i < 2u && i < q_loads; ++i) {
-        const uint32_t last = q_loads - 1u - i;  // the last Q load of each slot
-        drain_bar(sm, kBarQFull + (int)(last & 1u), (last >> 1) & 1u, p);
+    for (uint32_t i = 0; i < (uint32_t)kQSlots && i < q_loads; ++i) {
+        const uint32_t last = q_loads - 1u - i;
+        drain_bar(sm, kBarQFull + (int)(last % kQSlots), (last / kQSlots) & 1u, p);
     }
 }
 
@@ -385,8 +442,8 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
     };
     for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x, ++uu) {
         const int head = unit / p.pairs, pr = unit % p.pairs;
-        const uint32_t qs = uu & 1u;
-        ok = wait_bar(sm, kBarQFull + (int)qs, (uu >> 1) & 1u, p, kWhereQFull);
+        const uint32_t qs = uu % kQSlots;
+        ok = wait_bar(sm, kBarQFull + (int)qs, (uu / kQSlots) & 1u, p, kWhereQFull);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint64_t qd = q0 + qs * kDescTile;
@@ -446,63 +503,67 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Column c of a K/V tile is visible to the warp when bit (c % 32) of
-// mk[c / 32] is set.  Chunks with mk == 0 are skipped; kMasked tests single
-// columns (only edge tiles with missing tokens need it).
+// One 64-key half of a K/V tile: s[c][i] is the score of key 32 c + i of the
+// half, visible to the warp when bit i of w[c] is set.  kMasked tests single
+// keys (only tiles on the grid's edge, with missing tokens, need it).
 template <bool kMasked>
-__device__ __forceinline__ float row_max(const uint32_t (&s)[4][32], const uint32_t (&mk)[4]) {
+__device__ __forceinline__ float half_max(const uint32_t (&s)[2][32], const uint32_t (&w)[2]) {
     float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-        if (mk[c4] == 0u) continue;
+    for (int c = 0; c < 2; ++c) {
         if (!kMasked) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
-                m0 = ptx::max3(m0, u2f(s[c4][i]), u2f(s[c4][i + 1]));
-                m1 = ptx::max3(m1, u2f(s[c4][i + 2]), u2f(s[c4][i + 3]));
+                m0 = ptx::max3(m0, u2f(s[c][i]), u2f(s[c][i + 1]));
+                m1 = ptx::max3(m1, u2f(s[c][i + 2]), u2f(s[c][i + 3]));
             }
         } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-                if ((mk[c4] >> i) & 1u) m0 = fmaxf(m0, u2f(s[c4][i]));
+                if ((w[c] >> i) & 1u) m0 = fmaxf(m0, u2f(s[c][i]));
         }
     }
     return fmaxf(m0, m1);
 }
 
+// p = 2^(s * scale_log2 - m) for the half's 64 keys, as 32 packed bf16 pairs
+// at TMEM address t_p; returns the float32 sum of p.
 template <bool kMasked>
-__device__ __forceinline__ float write_probs(const uint32_t (&s)[4][32], const uint32_t (&mk)[4], float scale_log2,
-                                             float m, uint32_t t_s) {
+__device__ __forceinline__ float half_probs(const uint32_t (&s)[2][32], const uint32_t (&w)[2], float scale_log2,
+                                            float m, uint32_t t_p) {
     float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
+    for (int c = 0; c < 2; ++c) {
         uint32_t pk[16];
-        if (mk[c4] == 0u) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = 0u;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                float x0, x1, x2, x3;
-                ptx::fma2(x0, x1, u2f(s[c4][i]), u2f(s[c4][i + 1]), scale_log2, -m);
-                ptx::fma2(x2, x3, u2f(s[c4][i + 2]), u2f(s[c4][i + 3]), scale_log2, -m);
-                float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
-                float p2 = ptx::ex2_approx(x2), p3 = ptx::ex2_approx(x3);
-                if (kMasked) {
-                    p0 = ((mk[c4] >> i) & 1u) ? p0 : 0.f;
-                    p1 = ((mk[c4] >> (i + 1)) & 1u) ? p1 : 0.f;
-                    p2 = ((mk[c4] >> (i + 2)) & 1u) ? p2 : 0.f;
-                    p3 = ((mk[c4] >> (i + 3)) & 1u) ? p3 : 0.f;
-                }
-                ptx::add2(a0, a1, p0, p1);
-                ptx::add2(b0, b1, p2, p3);
-                pk[i / 2] = pack_bf16x2(p0, p1);
-                pk[i / 2 + 1] = pack_bf16x2(p2, p3);
+        for (int i = 0; i < 32; i += 4) {
+            float x0, x1, x2, x3;
+            ptx::fma2(x0, x1, u2f(s[c][i]), u2f(s[c][i + 1]), scale_log2, -m);
+            ptx::fma2(x2, x3, u2f(s[c][i + 2]), u2f(s[c][i + 3]), scale_log2, -m);
+            float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
+            float p2 = ptx::ex2_approx(x2), p3 = ptx::ex2_approx(x3);
+            if (kMasked) {
+                p0 = ((w[c] >> i) & 1u) ? p0 : 0.f;
+                p1 = ((w[c] >> (i + 1)) & 1u) ? p1 : 0.f;
+                p2 = ((w[c] >> (i + 2)) & 1u) ? p2 : 0.f;
+                p3 = ((w[c] >> (i + 3)) & 1u) ? p3 : 0.f;
             }
+            ptx::add2(a0, a1, p0, p1);
+            ptx::add2(b0, b1, p2, p3);
+            pk[i / 2] = pack_bf16x2(p0, p1);
+            pk[i / 2 + 1] = pack_bf16x2(p2, p3);
         }
-        ptx::tmem_st_32x32b_x16(t_s + (uint32_t)(c4 * 16), pk);
+        ptx::tmem_st_32x32b_x16(t_p + (uint32_t)(c * 16), pk);
     }
     return (a0 + a1) + (b0 + b1);
+}
+
+__device__ __forceinline__ void zero_half(uint32_t t_p) {
+    uint32_t zero[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) zero[i] = 0u;
+    ptx::tmem_st_32x32b_x16(t_p, zero);
+    ptx::tmem_st_32x32b_x16(t_p + 16u, zero);
 }
 
 // Softmax warpgroup k (0 or 1); thread t owns row t of the Q tile.
@@ -515,54 +576,70 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
     bool ok = true;
     for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x, ++uu) {
         const int head = unit / p.pairs, pr = unit % p.pairs;
-        const int32_t *lst = p.lists + ((size_t)head * p.pairs + pr) * 2 * p.topk;
+        const int32_t *lst = p.lists + ((size_t)head * p.pairs + pr) * p.list_ld;
         const int cnt = p.counts[(size_t)head * p.pairs + pr];
         const int nkv = (cnt + 1) / 2;
+        MaskWindow win;
+        win.init(lst, cnt, t & 31, qhalf, &p.g);
         float m_used = -INFINITY, l = 0.f;
         for (int j = k; j < nkv; j += 2) {
+            uint32_t mk[4];
+            win.tile(j, mk);
             ok = __all_sync(0xffffffffu, wait_bar(sm, kBarSFull + k, seen & 1u, p, kWhereSFull));
             if (!ok) break;
             ++seen;
             ptx::tc_fence_after();
-            const int e0 = entry(lst, cnt, 2 * j), e1 = entry(lst, cnt, 2 * j + 1);
-            const uint64_t v0 = ((e0 >> (16 + qhalf)) & 1) ? tile_token_mask(p.g, e0 & 0xFFFF) : 0ull;
-            const uint64_t v1 = (2 * j + 1 < cnt && ((e1 >> (16 + qhalf)) & 1)) ? tile_token_mask(p.g, e1 & 0xFFFF)
-                                                                                : 0ull;
-            const uint32_t mk[4] = {(uint32_t)v0, (uint32_t)(v0 >> 32), (uint32_t)v1, (uint32_t)(v1 >> 32)};
-            if ((mk[0] | mk[1] | mk[2] | mk[3]) == 0u) {
-                uint32_t zero[16];
+            // The two 64-key halves one after the other, each with only its own
+            // scores in registers.  P (bf16 pairs) of half h goes to columns
+            // [32 h, 32 h + 32) of S: half 1's P overwrites scores of half 0,
+            // which by then are consumed; half 1's scores (columns 64-127) are
+            // never overwritten.
+            float factor = 1.f;  // rescale of O accumulated before this tile
 #pragma unroll
-                for (int i = 0; i < 16; ++i) zero[i] = 0u;
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) ptx::tmem_st_32x32b_x16(t_s + (uint32_t)(c4 * 16), zero);
-                ptx::tmem_st_wait();
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(sm.b(kBarPFull + k));
-                continue;
-            }
-            uint32_t s[4][32];
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) ptx::tmem_ld_32x32b_x32(t_s + (uint32_t)(32 * c4), s[c4]);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) ptx::reg_fence(s[c4]);
-            bool partial = false;
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) partial |= mk[c4] != 0u && mk[c4] != 0xFFFFFFFFu;
-            const float m_tile = (partial ? row_max<true>(s, mk) : row_max<false>(s, mk)) * p.scale_log2;
-            float factor = 1.f;
-            bool rescale = false;
-            if (m_tile > m_used + kRescaleThreshold) {
-                if (m_used != -INFINITY) {
-                    factor = ptx::ex2_approx(m_used - m_tile);
-                    rescale = true;
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t w[2] = {mk[2 * h], mk[2 * h + 1]};
+                const uint32_t t_p = t_s + 32u * (uint32_t)h;
+                if ((w[0] | w[1]) == 0u) {
+                    zero_half(t_p);
+                    continue;
                 }
-                m_used = m_tile;
+                uint32_t sc[2][32];
+                ptx::tmem_ld_32x32b_x32(t_s + 64u * (uint32_t)h, sc[0]);
+                ptx::tmem_ld_32x32b_x32(t_s + 64u * (uint32_t)h + 32u, sc[1]);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence(sc[0]);
+                ptx::reg_fence(sc[1]);
+                const bool full = (w[0] & w[1]) == 0xFFFFFFFFu;
+                const float mh = (full ? half_max<false>(sc, w) : half_max<true>(sc, w)) * p.scale_log2;
+                float f = 1.f;
+                if (mh > m_used + kRescaleThreshold) {
+                    if (m_used != -INFINITY) f = ptx::ex2_approx(m_used - mh);
+                    m_used = mh;
+                }
+                l *= f;
+                factor *= f;
+                // half 1 raised the maximum: half 0's P, already written with
+                // the old one, takes the same factor (rare; warp-collective)
+                if (h == 1 && (mk[0] | mk[1]) != 0u && __any_sync(0xffffffffu, f != 1.f)) {
+                    uint32_t pp[32];
+                    ptx::tmem_st_wait();
+                    ptx::tmem_ld_32x32b_x32(t_s, pp);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence(pp);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&pp[i]);
+                        const float2 fv = __bfloat1622float2(v);
+                        pp[i] = pack_bf16x2(fv.x * f, fv.y * f);
+                    }
+                    ptx::tmem_st_32x32b_x32(t_s, pp);
+                }
+                l += full ? half_probs<false>(sc, w, p.scale_log2, m_used, t_p)
+                          : half_probs<true>(sc, w, p.scale_log2, m_used, t_p);
             }
-            const float tile_sum = partial ? write_probs<true>(s, mk, p.scale_log2, m_used, t_s)
-                                           : write_probs<false>(s, mk, p.scale_log2, m_used, t_s);
-            l = l * factor + tile_sum;
-            if (__any_sync(0xffffffffu, rescale)) {
+            // O holds nothing of this unit before the group's first tile (and the
+            // other group may still be reading the previous unit's O there)
+            if (j != k && __any_sync(0xffffffffu, factor != 1.f)) {
 #pragma unroll 1
                 for (int c4 = 0; c4 < 4; ++c4) {
                     uint32_t o[32];
@@ -662,9 +739,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(sm.b(kBarKvFull + s), 1);
             ptx::mbar_init(sm.b(kBarKvEmpty + s), 1);
         }
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < kQSlots; ++k) {
             ptx::mbar_init(sm.b(kBarQFull + k), 1);
             ptx::mbar_init(sm.b(kBarQEmpty + k), 1);
+        }
+        for (int k = 0; k < 2; ++k) {
             ptx::mbar_init(sm.b(kBarSFull + k), 1);
             ptx::mbar_init(sm.b(kBarPFull + k), 128);
             ptx::mbar_init(sm.b(kBarOFull + k), 1);
@@ -689,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
     if (warp == kTmaWarp) {
-        if (lane == 0) producer(&tm_q, &tm_k, &tm_v, p, sm);
+        producer(&tm_q, &tm_k, &tm_v, p, sm, lane);
     } else if (warp == kMmaWarp) {
         if (lane == 0) mma_issuer(p, sm, tmem);
     } else {
@@ -805,7 +884,7 @@ fv_status launch_vsa_attn(const VsaLaunch &a, cudaStream_t stream) {
     p.ld = ld;
     p.pairs = pairs;
     p.num_units = a.heads * pairs;
-    p.topk = a.topk;
+    p.list_ld = 2 * a.topk;
     p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
     const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
     vsa_fine_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
