@@ -29,6 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import workloads as W  # noqa: E402
@@ -345,6 +346,47 @@ def run_fv(args):
                      "gflop": flops / 1e9, "tflops": flops / (dms / 1e3) / 1e12,
                      "vdn_hybrid_ms": (window["ms"] + dms) if window else None}
 
+        # ---- VSA-style block-sparse attention: (4, 4, 4) tiles of the latent
+        # grid, 90% sparsity, on the same Q, K, V
+        vsa = None
+        if not args.no_window and w.n % W.tokens_per_latent_frame(1344, 768) == 0:
+            lat_h, lat_w = 768 // 32, 1344 // 32
+            frames = w.n // (lat_h * lat_w)
+            nt = fv.vsa_num_tiles(frames, lat_h, lat_w)
+            topk = fv.vsa_topk(nt, 0.9)
+            ov = torch.empty_like(q)
+            sel = torch.empty((w.heads, nt, topk), dtype=torch.int32, device=dev)
+            wsv = torch.empty(fv.load_library().fv_vsa_workspace_bytes(w.heads, frames, lat_h, lat_w, topk),
+                              dtype=torch.uint8, device=dev)
+
+            def run_vsa():
+                fv.vsa_attn(q, k, v, frames=frames, height=lat_h, width=lat_w, topk=topk, out=ov, selected=sel,
+                            workspace=wsv, stream=stream)
+
+            for _ in range(2):
+                run_vsa()
+            reps = 5
+            v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            v0.record(stream)
+            for _ in range(reps):
+                run_vsa()
+            v1.record(stream)
+            torch.cuda.synchronize(dev)
+            fv.sync_status(stream)
+            vms = v0.elapsed_time(v1) / reps
+            # useful work: every query against the real tokens of its kept tiles
+            tw, th = (lat_w + 3) // 4, (lat_h + 3) // 4
+            b = np.arange(nt)
+            sizes = (np.minimum(4, lat_w - 4 * (b % tw)) * np.minimum(4, lat_h - 4 * ((b // tw) % th))
+                     * np.minimum(4, frames - 4 * (b // (tw * th))))
+            kept = sizes[sel.cpu().numpy()].sum(axis=2)
+            flops = 4.0 * W.HEAD_DIM * float((kept * sizes[None, :]).sum())
+            vsa = {"kernels": "vsa_pool, vsa_select, vsa_fine", "grid": [frames, lat_h, lat_w], "tiles": nt,
+                   "topk": topk, "sparsity": 0.9, "ms": vms, "useful_tflop": flops / 1e12,
+                   "effective_tflops": flops / (vms / 1e3) / 1e12,
+                   "speedup_vs_dense": (sum(attn_ms) / len(attn_ms)) / vms}
+
         # ---- end to end through the C ABI: pinned host inputs in, results out.
         # Every step copies its own inputs host->device and reads its results
         # back; copies run on their own streams, double-buffered, so step i's
@@ -449,6 +491,7 @@ def run_fv(args):
         "elementwise_ms_per_step": (ms_total / args.steps) - attn_avg_ms,
         "vdn_window_attention": window,
         "vdn_delta_attention": delta,
+        "vsa_block_sparse_attention": vsa,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
