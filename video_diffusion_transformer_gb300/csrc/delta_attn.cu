@@ -12,13 +12,13 @@
 //             softmax window and n = (c + W + 1) C (clamped to F-1) the first
 //             frame after it.
 //
-// Four kernels, float32 on the CUDA cores:
-//   stats   (frame, head): I + A_t -> ws_m, B_t -> ws_c
-//   solve   (frame, head): Gauss-Jordan on [I + A_t | B_t^T] in registers,
+// Four kernels:
+//   stats   (frame, head; tensor cores, delta_tc.cu): I + A_t -> ws_m, B_t -> ws_c
+//   solve   (frame, head; float32): Gauss-Jordan on [I + A_t | B_t^T] in registers,
 //                          M'_t = Diag(alpha_t) (I + A_t)^{-1} -> ws_m,
 //                          C_t = B_t (I + A_t)^{-1} -> ws_c
-//   scan    (head, direction): S <- S M'_t + C_t, frame by frame
-//   readout (frame, head): o = (S_fwd[p] + S_rev[n]) q_hat, rounded to bf16
+//   scan    (head, direction; float32): S <- S M'_t + C_t, frame by frame
+//   readout (frame, head; float32): o = (S_fwd[p] + S_rev[n]) q_hat, rounded to bf16
 // The scan is the only sequential part: 2 H chains of F - 2 128x128x128 steps.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -32,91 +32,9 @@ namespace {
 
 constexpr int kDv = 128;          // key and value dimension of a head
 constexpr int kDThreads = 256;    // 16 x 16 threads, each an 8 x 8 block of a 128 x 128 result
-constexpr int kTokBlock = 32;     // tokens staged per step of the statistics kernel
 constexpr size_t kMat = (size_t)kDv * kDv;
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-// ------------------------------------------------------------------ stats
-// I + A and B of frame t of head h.  Shared memory: normalised keys, beta
-// times normalised keys, and values of kTokBlock tokens.
-__global__ void __launch_bounds__(kDThreads, 1)
-    vda_stats_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
-                     const float *__restrict__ beta, int64_t n, int ld, int frame_tokens, float *__restrict__ ws_m,
-                     float *__restrict__ ws_c) {
-    const int t = (int)blockIdx.x + 1;  // frames 1 .. F-2
-    const int h = (int)blockIdx.y;
-    const int frames = (int)(n / frame_tokens);
-    __shared__ __align__(16) float kh[kTokBlock][kDv];
-    __shared__ __align__(16) float bk[kTokBlock][kDv];
-    __shared__ __align__(16) float vs[kTokBlock][kDv];
-    const int tid = (int)threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int ty = tid >> 4, tx = tid & 15;
-    float acc_a[8][8], acc_b[8][8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc_a[i][j] = acc_b[i][j] = 0.f;
-    const int64_t tok0 = (int64_t)t * frame_tokens;
-    for (int u0 = 0; u0 < frame_tokens; u0 += kTokBlock) {
-        // stage: warp w normalises tokens w, w + 8, w + 16, w + 24 of the block
-        for (int r = warp; r < kTokBlock; r += kDThreads / 32) {
-            const int u = u0 + r;
-            float kk[4], vv[4];
-            float ss = 0.f, b = 0.f;
-            if (u < frame_tokens) {
-                const int64_t row = (tok0 + u) * (int64_t)ld + (int64_t)h * kDv + lane * 4;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    kk[e] = bf2f(k[row + e]);
-                    vv[e] = bf2f(v[row + e]);
-                    ss = fmaf(kk[e], kk[e], ss);
-                }
-                b = beta[(int64_t)h * n + tok0 + u];
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) kk[e] = vv[e] = 0.f;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                kh[r][lane * 4 + e] = kk[e] * inv;
-                bk[r][lane * 4 + e] = kk[e] * inv * b;
-                vs[r][lane * 4 + e] = vv[e];
-            }
-        }
-        __syncthreads();
-#pragma unroll 2
-        for (int r = 0; r < kTokBlock; ++r) {
-            float ki[8], vi[8], bj[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                ki[i] = kh[r][ty * 8 + i];
-                vi[i] = vs[r][ty * 8 + i];
-                bj[i] = bk[r][tx * 8 + i];
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    acc_a[i][j] = fmaf(ki[i], bj[j], acc_a[i][j]);
-                    acc_b[i][j] = fmaf(vi[i], bj[j], acc_b[i][j]);
-                }
-        }
-        __syncthreads();
-    }
-    const size_t base = ((size_t)h * frames + t) * kMat;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int r = ty * 8 + i, c = tx * 8 + j;
-            ws_m[base + (size_t)r * kDv + c] = acc_a[i][j] + (r == c ? 1.0f : 0.0f);
-            ws_c[base + (size_t)r * kDv + c] = acc_b[i][j];
-        }
-}
 
 // ------------------------------------------------------------------ solve
 // Gauss-Jordan elimination on the 128 x 256 matrix [I + A | B^T] of frame t
@@ -418,14 +336,12 @@ fv_status launch_delta_attn(const DeltaLaunch &a, cudaStream_t stream) {
             cudaSuccess)
         return FV_ERR_LAUNCH;
     const auto *q = static_cast<const __nv_bfloat16 *>(a.q);
-    const auto *k = static_cast<const __nv_bfloat16 *>(a.k);
-    const auto *v = static_cast<const __nv_bfloat16 *>(a.v);
     float *ws_m = a.workspace;
     float *ws_c = a.workspace + (size_t)a.heads * frames * kMat;
     if (frames > 2) {
-        const dim3 g(frames - 2, a.heads);
-        vda_stats_kernel<<<g, kDThreads, 0, stream>>>(k, v, a.beta, a.n, ld, a.frame_tokens, ws_m, ws_c);
-        vda_solve_kernel<<<g, kDThreads, 0, stream>>>(a.alpha, frames, ws_m, ws_c);
+        const fv_status st = launch_vda_stats_tc(a, ws_m, ws_c, stream);
+        if (st != FV_OK) return st;
+        vda_solve_kernel<<<dim3(frames - 2, a.heads), kDThreads, 0, stream>>>(a.alpha, frames, ws_m, ws_c);
     }
     vda_scan_kernel<<<dim3(a.heads, 2), kDThreads, scan_smem, stream>>>(a.text_state, frames, ws_m, ws_c, a.states);
     vda_readout_kernel<<<dim3(frames, a.heads), kDThreads, read_smem, stream>>>(

@@ -1,0 +1,385 @@
+// Video Delta Attention on the tensor cores: the per-frame sums of the
+// linear branch ("FreeVideo: a 66 GB video transformer on an 8 GB card",
+// section "Where Video DeltaNet comes in"), per frame t and head h,
+//   A_t = sum_u beta_u k_hat_u k_hat_u^T = K^T Diag(beta / |k|^2) K
+//   B_t = sum_u beta_u v_u k_hat_u^T     = (Diag(beta / |k|) V)^T K
+// over the frame's tokens u (k_hat = k / |k|).  Each product has one exact
+// bf16 operand (K) and one scaled operand, which is split into bf16 hi + lo
+// parts (x = hi + lo to about 2^-16 relative), so two bf16 MMAs with float32
+// accumulation give the sums to about float32 accuracy.
+//
+// vda_stats_tc (persistent, one CTA per SM, 320 threads): unit = (frame, head).
+//   warp 8 (one thread): TMA loads of 64-token stages, K and V as 64 x 64
+//     bf16 boxes in the 128-byte swizzled layout, two stages in flight;
+//   warps 4-7 (the scalers): thread = (token, channel half); squared norm of
+//     k over both halves, then w_A k and w_B v split into hi and lo, written
+//     to the same (swizzled) byte positions of their own buffers (v's hi
+//     over v itself), so every operand shares K's layout;
+//   warp 9 (one thread): per 16 tokens, D_A += K^T (w_A K)_hi, D_A += K^T
+//     (w_A K)_lo, D_B += (w_B V)_hi^T K, D_B += (w_B V)_lo^T K, both operands
+//     MN-major (channels contiguous); D_A and D_B in tensor memory, double
+//     buffered across units;
+//   warps 0-3 (the epilogue): thread = row i of D; writes row i of I + A_t and
+//     of B_t (float32) to the workspace.
+// All waits are bounded; a wait that runs out records kDevTimeout | where.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "fv_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fv {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTok = 64;                       // tokens per stage
+constexpr int kHalf = kTok * 64 * 2;           // one 64-token x 64-channel box (8 KB)
+constexpr int kOperand = 2 * kHalf;            // 64 tokens x 128 channels (16 KB)
+// stage layout: K, V (overwritten by (w_B V)_hi), (w_B V)_lo, (w_A K)_hi, (w_A K)_lo
+constexpr int kOffK = 0, kOffVHi = kOperand, kOffVLo = 2 * kOperand, kOffXHi = 3 * kOperand, kOffXLo = 4 * kOperand;
+constexpr int kStageBytes = 5 * kOperand;      // 80 KB
+constexpr int kStages = 2;
+constexpr int kThreads = 320;
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;            // 2 buffers x (D_A, D_B)
+
+constexpr int kBarKvFull = 0;                  // TMA -> scalers
+constexpr int kBarXFull = kBarKvFull + kStages;     // scalers -> MMA (128 arrivals)
+constexpr int kBarStageEmpty = kBarXFull + kStages;  // MMA -> producer
+constexpr int kBarAccFull = kBarStageEmpty + kStages;  // MMA -> epilogue
+constexpr int kBarAccEmpty = kBarAccFull + 2;  // epilogue -> MMA (128 arrivals)
+constexpr int kBarDrain = kBarAccEmpty + 2;
+constexpr int kNumBars = kBarDrain + 1;
+
+constexpr int kSmemStages = 0;
+constexpr int kSmemBar = kSmemStages + kStages * kStageBytes;
+constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
+constexpr int kSmemBytes = kSmemMisc + 16 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+constexpr int kWhereStageEmpty = 1, kWhereKvFull = 2, kWhereXFull = 3, kWhereAccEmpty = 4, kWhereAccFull = 5,
+              kWhereDrain = 6;
+
+struct Params {
+    const float *beta;  // [heads, n]
+    float *ws_m, *ws_c; // [heads, frames, 128, 128]
+    int *status;
+    int n, heads, frames, frame_tokens;
+    int stages;         // stages per frame: ceil(frame_tokens / 64)
+    int num_units;      // (frames - 2) * heads
+};
+
+struct Smem {
+    uint32_t stages, bar;
+    volatile int *abort_flag;
+    __device__ uint32_t b(int i) const { return bar + 8u * (uint32_t)i; }
+};
+
+__device__ __forceinline__ bool wait_bar(const Smem &sm, int i, uint32_t parity, const Params &p, int where) {
+    return ptx::mbar_wait(sm.b(i), parity, sm.abort_flag, p.status, kDevTimeout | where);
+}
+
+__device__ __forceinline__ void drain_bar(const Smem &sm, int i, uint32_t parity, const Params &p) {
+    int never = 0;
+    ptx::mbar_wait(sm.b(i), parity, &never, p.status, kDevTimeout | kWhereDrain);
+}
+
+// unit -> (frame 1 .. F-2, head); heads innermost so the CTAs running together
+// read the same token rows
+__device__ __forceinline__ void unit_of(const Params &p, int unit, int &frame, int &head) {
+    frame = 1 + unit / p.heads;
+    head = unit % p.heads;
+}
+
+__device__ void producer(const CUtensorMap *tk, const CUtensorMap *tv, const Params &p, const Smem &sm) {
+    uint32_t g = 0;  // stages issued
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
+        int frame, head;
+        unit_of(p, unit, frame, head);
+        for (int s = 0; ok && s < p.stages; ++s, ++g) {
+            const uint32_t slot = g % kStages;
+            ok = wait_bar(sm, kBarStageEmpty + (int)slot, ((g / kStages) & 1u) ^ 1u, p, kWhereStageEmpty);
+            if (!ok) break;
+            const uint32_t base = sm.stages + slot * (uint32_t)kStageBytes;
+            const int row = frame * p.frame_tokens + s * kTok;
+            ptx::mbar_arrive_expect_tx(sm.b(kBarKvFull + (int)slot), 2 * kOperand);
+            for (int c = 0; c < 2; ++c) {
+                ptx::tma_load_2d(base + kOffK + c * kHalf, tk, sm.b(kBarKvFull + (int)slot), head * kD + 64 * c, row);
+                ptx::tma_load_2d(base + kOffVHi + c * kHalf, tv, sm.b(kBarKvFull + (int)slot), head * kD + 64 * c,
+                                 row);
+            }
+        }
+    }
+    for (uint32_t i = 0; i < (uint32_t)kStages && i < g; ++i) {
+        const uint32_t last = g - 1u - i;
+        drain_bar(sm, kBarKvFull + (int)(last % kStages), (last / kStages) & 1u, p);
+    }
+}
+
+__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bfloat16 &lo) {
+    hi = __float2bfloat16_rn(x);
+    lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
+// Scaler thread t (0..127): token u = t / 2 of the stage, channel half c = t % 2.
+__device__ void scaler(const Params &p, const Smem &sm, uint8_t *smem_stages, int t) {
+    const int u = t >> 1, c = t & 1;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
+        int frame, head;
+        unit_of(p, unit, frame, head);
+        for (int s = 0; ok && s < p.stages; ++s, ++g) {
+            const uint32_t slot = g % kStages;
+            const int tok = s * kTok + u;  // token within the frame
+            const float beta = tok < p.frame_tokens
+                                   ? p.beta[(size_t)head * p.n + (size_t)frame * p.frame_tokens + tok]
+                                   : 0.0f;
+            ok = __all_sync(0xffffffffu, wait_bar(sm, kBarKvFull + (int)slot, (g / kStages) & 1u, p, kWhereKvFull));
+            if (!ok) break;
+            uint8_t *st = smem_stages + (size_t)slot * kStageBytes;
+            const int row_off = c * kHalf + u * 128;
+            // the row's eight 16-byte chunks, visited from a lane-dependent
+            // start so the eight lanes of a quarter-warp hit eight banks groups
+            uint4 kc[8];
+            float ss = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int pos = (q + t) & 7;
+                kc[q] = *reinterpret_cast<const uint4 *>(st + kOffK + row_off + pos * 16);
+                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&kc[q]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(h2[e]);
+                    ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+                }
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);  // the other channel half of the token
+            const float wa = beta / fmaxf(ss, 1e-24f);
+            const float wb = beta / fmaxf(sqrtf(ss), 1e-12f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int pos = (q + t) & 7;
+                const int off = row_off + pos * 16;
+                const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kc[q]);
+                const uint4 vc = *reinterpret_cast<const uint4 *>(st + kOffVHi + off);
+                const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&vc);
+                uint4 xh, xl, vh, vl;
+                __nv_bfloat16 *xh_ = reinterpret_cast<__nv_bfloat16 *>(&xh);
+                __nv_bfloat16 *xl_ = reinterpret_cast<__nv_bfloat16 *>(&xl);
+                __nv_bfloat16 *vh_ = reinterpret_cast<__nv_bfloat16 *>(&vh);
+                __nv_bfloat16 *vl_ = reinterpret_cast<__nv_bfloat16 *>(&vl);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 kf = __bfloat1622float2(k2[e]), vf = __bfloat1622float2(v2[e]);
+                    split_bf16(wa * kf.x, xh_[2 * e], xl_[2 * e]);
+                    split_bf16(wa * kf.y, xh_[2 * e + 1], xl_[2 * e + 1]);
+                    split_bf16(wb * vf.x, vh_[2 * e], vl_[2 * e]);
+                    split_bf16(wb * vf.y, vh_[2 * e + 1], vl_[2 * e + 1]);
+                }
+                *reinterpret_cast<uint4 *>(st + kOffXHi + off) = xh;
+                *reinterpret_cast<uint4 *>(st + kOffXLo + off) = xl;
+                *reinterpret_cast<uint4 *>(st + kOffVHi + off) = vh;
+                *reinterpret_cast<uint4 *>(st + kOffVLo + off) = vl;
+            }
+            // the tensor core reads these through the async proxy
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            ptx::mbar_arrive(sm.b(kBarXFull + (int)slot));
+        }
+    }
+}
+
+constexpr uint64_t kDescStage = (uint64_t)(kStageBytes >> 4);
+
+__device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
+    // MN-major operands: channel halves 8 KB apart (leading offset), 8-token
+    // groups 1 KB apart (stride offset); 16 tokens per MMA = 2 KB
+    const uint64_t dk = ptx::sdesc_sw128(sm.stages + kOffK, kHalf, 1024);
+    const uint64_t dvh = ptx::sdesc_sw128(sm.stages + kOffVHi, kHalf, 1024);
+    const uint64_t dvl = ptx::sdesc_sw128(sm.stages + kOffVLo, kHalf, 1024);
+    const uint64_t dxh = ptx::sdesc_sw128(sm.stages + kOffXHi, kHalf, 1024);
+    const uint64_t dxl = ptx::sdesc_sw128(sm.stages + kOffXLo, kHalf, 1024);
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, true, true);
+    uint32_t g = 0, units = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x, ++units) {
+        const uint32_t buf = units & 1u;
+        ok = wait_bar(sm, kBarAccEmpty + (int)buf, ((units >> 1) & 1u) ^ 1u, p, kWhereAccEmpty);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t d_a = tmem + 256u * buf, d_b = d_a + 128u;
+        for (int s = 0; ok && s < p.stages; ++s, ++g) {
+            const uint32_t slot = g % kStages;
+            ok = wait_bar(sm, kBarXFull + (int)slot, (g / kStages) & 1u, p, kWhereXFull);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint64_t so = slot * kDescStage;
+#pragma unroll
+            for (int kk = 0; kk < kTok / 16; ++kk) {
+                const uint64_t off = so + (uint64_t)((kk * 16 * 128) >> 4);
+                const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+                ptx::mma_ss(d_a, dk + off, dxh + off, idesc, acc);
+                ptx::mma_ss(d_a, dk + off, dxl + off, idesc, 1u);
+                ptx::mma_ss(d_b, dvh + off, dk + off, idesc, acc);
+                ptx::mma_ss(d_b, dvl + off, dk + off, idesc, 1u);
+            }
+            ptx::tc_commit(sm.b(kBarStageEmpty + (int)slot));
+        }
+        if (!ok) break;
+        ptx::tc_commit(sm.b(kBarAccFull + (int)buf));
+    }
+    ptx::tc_commit(sm.b(kBarDrain));
+    drain_bar(sm, kBarDrain, 0u, p);
+}
+
+// Epilogue thread t owns row t of D_A and D_B.
+__device__ void epilogue(const Params &p, const Smem &sm, uint32_t tmem, int t) {
+    const uint32_t lane_base = (uint32_t)((t >> 5) * 32) << 16;
+    uint32_t units = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x, ++units) {
+        int frame, head;
+        unit_of(p, unit, frame, head);
+        const uint32_t buf = units & 1u;
+        ok = __all_sync(0xffffffffu, wait_bar(sm, kBarAccFull + (int)buf, (units >> 1) & 1u, p, kWhereAccFull));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const size_t base = (((size_t)head * p.frames + frame) * kD + t) * kD;
+        for (int m = 0; m < 2; ++m) {
+            float *dst = (m == 0 ? p.ws_m : p.ws_c) + base;
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(tmem + lane_base + 256u * buf + 128u * (uint32_t)m + 32u * (uint32_t)c4, r);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence(r);
+                if (m == 0 && (t >> 5) == c4) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (e == (t & 31)) r[e] = __float_as_uint(__uint_as_float(r[e]) + 1.0f);
+                }
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    *reinterpret_cast<uint4 *>(dst + 32 * c4 + 4 * v) =
+                        make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+            }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(sm.b(kBarAccEmpty + (int)buf));
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    vda_stats_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                        const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    Smem sm;
+    sm.stages = base + kSmemStages;
+    sm.bar = base + kSmemBar;
+    sm.abort_flag = reinterpret_cast<volatile int *>(smem + kSmemMisc + 4);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + kSmemMisc);
+    const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(sm.b(kBarKvFull + s), 1);
+            ptx::mbar_init(sm.b(kBarXFull + s), 128);
+            ptx::mbar_init(sm.b(kBarStageEmpty + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(sm.b(kBarAccFull + b), 1);
+            ptx::mbar_init(sm.b(kBarAccEmpty + b), 128);
+        }
+        ptx::mbar_init(sm.b(kBarDrain), 1);
+        *sm.abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kTmaWarp && lane == 0) {
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
+    if (warp == kTmaWarp) {
+        if (lane == 0) producer(&tm_k, &tm_v, p, sm);
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) mma_issuer(p, sm, tmem);
+    } else if (warp >= 4) {
+        scaler(p, sm, smem + kSmemStages, (int)threadIdx.x - 128);
+    } else {
+        epilogue(p, sm, tmem, (int)threadIdx.x);
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// [n, ld] bf16 row-major, boxes of 64 rows x 64 columns, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t n, int ld) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)n};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2u};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)kTok};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+fv_status launch_vda_stats_tc(const DeltaLaunch &a, float *ws_m, float *ws_c, cudaStream_t stream) {
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FV_ERR_LAUNCH;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(vda_stats_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+                cudaSuccess)
+                return FV_ERR_LAUNCH;
+            attr_set[dev] = true;
+        }
+    }
+    const int frames = (int)(a.n / a.frame_tokens);
+    if (frames <= 2) return FV_OK;
+    const int ld = a.heads * kD;
+    CUtensorMap mk, mv;
+    if (!make_map(&mk, a.k, a.n, ld) || !make_map(&mv, a.v, a.n, ld)) return FV_ERR_LAUNCH;
+    Params p;
+    p.beta = a.beta;
+    p.ws_m = ws_m;
+    p.ws_c = ws_c;
+    p.status = a.status;
+    p.n = (int)a.n;
+    p.heads = a.heads;
+    p.frames = frames;
+    p.frame_tokens = a.frame_tokens;
+    p.stages = (a.frame_tokens + kTok - 1) / kTok;
+    p.num_units = (frames - 2) * a.heads;
+    const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
+    vda_stats_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
+}
+
+}  // namespace fv

@@ -160,6 +160,8 @@ fv_status fv_delta_attn(const void *Q, const void *K, const void *V, const float
     a.o = O;
     a.states = states;
     a.workspace = workspace;
+    a.status = d->status;
+    a.num_sms = d->num_sms;
     return fv::launch_delta_attn(a, static_cast<cudaStream_t>(stream));
 }
 

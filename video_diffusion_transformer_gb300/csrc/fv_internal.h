@@ -67,7 +67,13 @@ struct DeltaLaunch {
     void *o;                      // bf16 [n, heads * 128]
     float *states;                // [2, heads, frames, 128, 128]
     float *workspace;             // [2, heads, frames, 128, 128]
+    int *status;                  // device status word
+    int num_sms;
 };
+
+// The per-frame sums I + A_t -> ws_m and B_t -> ws_c of frames 1 .. F-2 on the
+// tensor cores (layout [heads, frames, 128, 128]).
+fv_status launch_vda_stats_tc(const DeltaLaunch &a, float *ws_m, float *ws_c, cudaStream_t stream);
 
 // Enqueue the Video Delta Attention kernels (stats, solve, scan, readout).
 fv_status launch_delta_attn(const DeltaLaunch &a, cudaStream_t stream);
