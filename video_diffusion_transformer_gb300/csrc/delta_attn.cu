@@ -18,7 +18,8 @@
 //                          M'_t = Diag(alpha_t) (I + A_t)^{-1} -> ws_m,
 //                          C_t = B_t (I + A_t)^{-1} -> ws_c
 //   scan    (head, direction; float32): S <- S M'_t + C_t, frame by frame
-//   readout (frame, head; float32): o = (S_fwd[p] + S_rev[n]) q_hat, rounded to bf16
+//   readout (chunk rows, head; tensor cores, delta_tc.cu): o = (S_fwd[p] + S_rev[n]) q_hat,
+//           rounded to bf16
 // The scan is the only sequential part: 2 H chains of F - 2 128x128x128 steps.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -34,7 +35,6 @@ constexpr int kDv = 128;          // key and value dimension of a head
 constexpr int kDThreads = 256;    // 16 x 16 threads, each an 8 x 8 block of a 128 x 128 result
 constexpr size_t kMat = (size_t)kDv * kDv;
 
-__device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 // ------------------------------------------------------------------ solve
 // Gauss-Jordan elimination on the 128 x 256 matrix [I + A | B^T] of frame t
@@ -260,82 +260,14 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
 }
 
-// ---------------------------------------------------------------- readout
-// o = (S_fwd[p] + S_rev[n]) q_hat for every token of frame t, head h.  The sum
-// is held transposed in shared memory, so lane l reads the four outputs
-// 4l .. 4l+3 of column q as one float4.
-__global__ void __launch_bounds__(kDThreads)
-    vda_readout_kernel(const __nv_bfloat16 *__restrict__ q, int64_t n, int ld, int frame_tokens, int chunk_frames,
-                       int window_chunks, const float *__restrict__ states, __nv_bfloat16 *__restrict__ o) {
-    extern __shared__ float sh[];
-    float *wt = sh;                    // [kDv][kDv]  (S_fwd[p] + S_rev[n])^T
-    float *qs = sh + kDv * kDv;        // [warps][kDv] normalised query of each warp
-    const int t = (int)blockIdx.x;
-    const int h = (int)blockIdx.y;
-    const int H = (int)gridDim.y;
-    const int frames = (int)(n / frame_tokens);
-    const int tid = (int)threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = t / chunk_frames;
-    int p = (c - window_chunks) * chunk_frames - 1;
-    p = p < 0 ? 0 : p;
-    int nx = (c + window_chunks + 1) * chunk_frames;
-    nx = nx > frames - 1 ? frames - 1 : nx;
-    const float *sf = states + ((size_t)h * frames + p) * kMat;
-    const float *sr = states + (((size_t)H + h) * frames + nx) * kMat;
-    for (int e = tid; e < kDv * kDv; e += kDThreads) {
-        const int r = e / kDv, col = e % kDv;
-        wt[col * kDv + r] = sf[e] + sr[e];
-    }
-    __syncthreads();
-    float *qw = qs + warp * kDv;
-    const int64_t tok0 = (int64_t)t * frame_tokens;
-    for (int u = warp; u < frame_tokens; u += kDThreads / 32) {
-        const int64_t row = (tok0 + u) * (int64_t)ld + (int64_t)h * kDv;
-        float qq[4], ss = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            qq[e] = bf2f(q[row + lane * 4 + e]);
-            ss = fmaf(qq[e], qq[e], ss);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) qw[lane * 4 + e] = qq[e] * inv;
-        __syncwarp();
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-        for (int k2 = 0; k2 < kDv; ++k2) {
-            const float qk = qw[k2];
-            const float4 w4 = *reinterpret_cast<const float4 *>(wt + k2 * kDv + lane * 4);
-            acc[0] = fmaf(w4.x, qk, acc[0]);
-            acc[1] = fmaf(w4.y, qk, acc[1]);
-            acc[2] = fmaf(w4.z, qk, acc[2]);
-            acc[3] = fmaf(w4.w, qk, acc[3]);
-        }
-        __syncwarp();
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2], acc[3]);
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t *>(&lo);
-        pk.y = *reinterpret_cast<uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(o + row + lane * 4) = pk;
-    }
-}
-
 }  // namespace
 
 fv_status launch_delta_attn(const DeltaLaunch &a, cudaStream_t stream) {
     const int frames = (int)(a.n / a.frame_tokens);
-    const int ld = a.heads * kDv;
     const size_t scan_smem = (size_t)(kDv * kSLd + 2 * kDv * kDv) * sizeof(float);
-    const size_t read_smem = (size_t)(kDv * kDv + (kDThreads / 32) * kDv) * sizeof(float);
     if (cudaFuncSetAttribute(vda_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(vda_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)read_smem) !=
-            cudaSuccess)
+        cudaSuccess)
         return FV_ERR_LAUNCH;
-    const auto *q = static_cast<const __nv_bfloat16 *>(a.q);
     float *ws_m = a.workspace;
     float *ws_c = a.workspace + (size_t)a.heads * frames * kMat;
     if (frames > 2) {
@@ -344,10 +276,9 @@ fv_status launch_delta_attn(const DeltaLaunch &a, cudaStream_t stream) {
         vda_solve_kernel<<<dim3(frames - 2, a.heads), kDThreads, 0, stream>>>(a.alpha, frames, ws_m, ws_c);
     }
     vda_scan_kernel<<<dim3(a.heads, 2), kDThreads, scan_smem, stream>>>(a.text_state, frames, ws_m, ws_c, a.states);
-    vda_readout_kernel<<<dim3(frames, a.heads), kDThreads, read_smem, stream>>>(
-        q, a.n, ld, a.frame_tokens, a.chunk_frames, a.window_chunks, a.states,
-        static_cast<__nv_bfloat16 *>(a.o));
-    return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
+    if (cudaGetLastError() != cudaSuccess) return FV_ERR_LAUNCH;
+    // the scan has consumed ws_m and ws_c: the readout's W splits reuse them
+    return launch_vda_readout_tc(a, reinterpret_cast<__nv_bfloat16 *>(a.workspace), stream);
 }
 
 }  // namespace fv

@@ -332,13 +332,281 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// [n, ld] bf16 row-major, boxes of 64 rows x 64 columns, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *ptr, int64_t n, int ld) {
+// ================================================================ readout
+// o = (S_fwd[p] + S_rev[n]) q / |q| for every token of chunk c, where p and n
+// are the frames just before and just after the chunk's softmax window.
+//
+// vda_wsplit (chunk, head): W = S_fwd[p] + S_rev[n] in float32, split into
+//   bf16 W_hi + W_lo ([heads, chunks, 2, 128, 128], rows i = output channel).
+// vda_readout_tc (persistent, 192 threads): unit = (128 query rows of one
+//   chunk, head), heads innermost.  Warp 4 (one thread) loads the Q tile and
+//   W_hi, W_lo by TMA (two stages of 96 KB); warp 5 (one thread) issues
+//   D = Q W_hi^T + Q W_lo^T (16 MMAs, both operands K-major, as Q K^T in the
+//   attention kernel); warps 0-3 (thread = row) take |q| from the Q tile in
+//   shared memory, then scale row t of D by 1 / max(|q|, 1e-12), round to bf16
+//   and store it if the row lies in the chunk.
+namespace ro {
+
+constexpr int kRows = 128;
+constexpr int kBox = kRows * 64 * 2;          // 128 rows x 64 channels (16 KB)
+constexpr int kTile = 2 * kBox;               // 32 KB
+constexpr int kOffQ = 0, kOffWHi = kTile, kOffWLo = 2 * kTile;
+constexpr int kStageBytes = 3 * kTile;        // 96 KB
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr int kTmaWarp = 4, kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 256;
+
+constexpr int kBarFull = 0;                   // TMA -> MMA and epilogue
+constexpr int kBarEmpty = kBarFull + kStages; // MMA commit + 128 epilogue arrivals -> producer
+constexpr int kBarAccFull = kBarEmpty + kStages;
+constexpr int kBarAccEmpty = kBarAccFull + 2;
+constexpr int kBarDrain = kBarAccEmpty + 2;
+constexpr int kNumBars = kBarDrain + 1;
+constexpr int kSmemBar = kStages * kStageBytes;
+constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
+constexpr int kSmemBytes = kSmemMisc + 16 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+constexpr int kWhereEmpty = 1, kWhereFull = 2, kWhereAccEmpty = 3, kWhereAccFull = 4, kWhereDrain = 5;
+
+struct Params {
+    __nv_bfloat16 *o;
+    int *status;
+    int n, ld, heads, chunk_tokens, chunks, tiles_per_chunk, num_units;
+};
+
+struct Smem {
+    uint32_t stages, bar;
+    volatile int *abort_flag;
+    __device__ uint32_t b(int i) const { return bar + 8u * (uint32_t)i; }
+};
+
+__device__ __forceinline__ bool wait_bar(const Smem &sm, int i, uint32_t parity, const Params &p, int where) {
+    return ptx::mbar_wait(sm.b(i), parity, sm.abort_flag, p.status, kDevTimeout | where);
+}
+
+__device__ __forceinline__ void drain_bar(const Smem &sm, int i, uint32_t parity, const Params &p) {
+    int never = 0;
+    ptx::mbar_wait(sm.b(i), parity, &never, p.status, kDevTimeout | kWhereDrain);
+}
+
+struct Unit {
+    int head, chunk, row0, row_end;  // rows [row0, min(row0 + 128, row_end)) are stored
+};
+
+__device__ __forceinline__ Unit unit_of(const Params &p, int unit) {
+    Unit u;
+    u.head = unit % p.heads;
+    const int tile = unit / p.heads;
+    u.chunk = tile / p.tiles_per_chunk;
+    u.row0 = u.chunk * p.chunk_tokens + (tile % p.tiles_per_chunk) * kRows;
+    u.row_end = min(p.n, (u.chunk + 1) * p.chunk_tokens);
+    return u;
+}
+
+__device__ void producer(const CUtensorMap *tq, const CUtensorMap *tw, const Params &p, const Smem &sm) {
+    uint32_t g = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x, ++g) {
+        const Unit u = unit_of(p, unit);
+        const uint32_t slot = g % kStages;
+        ok = wait_bar(sm, kBarEmpty + (int)slot, ((g / kStages) & 1u) ^ 1u, p, kWhereEmpty);
+        if (!ok) break;
+        const uint32_t base = sm.stages + slot * (uint32_t)kStageBytes;
+        const uint32_t bar = sm.b(kBarFull + (int)slot);
+        ptx::mbar_arrive_expect_tx(bar, kStageBytes);
+        const int wrow = (u.head * p.chunks + u.chunk) * 2 * kRows;
+        for (int c = 0; c < 2; ++c) {
+            ptx::tma_load_2d(base + kOffQ + c * kBox, tq, bar, u.head * 128 + 64 * c, u.row0);
+            ptx::tma_load_2d(base + kOffWHi + c * kBox, tw, bar, 64 * c, wrow);
+            ptx::tma_load_2d(base + kOffWLo + c * kBox, tw, bar, 64 * c, wrow + kRows);
+        }
+    }
+    for (uint32_t i = 0; i < (uint32_t)kStages && i < g; ++i) {
+        const uint32_t last = g - 1u - i;
+        drain_bar(sm, kBarFull + (int)(last % kStages), (last / kStages) & 1u, p);
+    }
+}
+
+constexpr uint64_t kDescStage = (uint64_t)(kStageBytes >> 4);
+
+__device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
+    const uint64_t dq = ptx::sdesc_sw128(sm.stages + kOffQ, 16, 1024);
+    const uint64_t dwh = ptx::sdesc_sw128(sm.stages + kOffWHi, 16, 1024);
+    const uint64_t dwl = ptx::sdesc_sw128(sm.stages + kOffWLo, 16, 1024);
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
+    uint32_t g = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x, ++g) {
+        const uint32_t slot = g % kStages, buf = g & 1u;
+        ok = wait_bar(sm, kBarAccEmpty + (int)buf, ((g >> 1) & 1u) ^ 1u, p, kWhereAccEmpty);
+        if (!ok) break;
+        ok = wait_bar(sm, kBarFull + (int)slot, (g / kStages) & 1u, p, kWhereFull);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint64_t so = slot * kDescStage;
+        const uint32_t d = tmem + 128u * buf;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t off = so + (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
+            ptx::mma_ss(d, dq + off, dwh + off, idesc, kk > 0 ? 1u : 0u);
+            ptx::mma_ss(d, dq + off, dwl + off, idesc, 1u);
+        }
+        ptx::tc_commit(sm.b(kBarEmpty + (int)slot));
+        ptx::tc_commit(sm.b(kBarAccFull + (int)buf));
+    }
+    ptx::tc_commit(sm.b(kBarDrain));
+    drain_bar(sm, kBarDrain, 0u, p);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ void epilogue(const Params &p, const Smem &sm, const uint8_t *smem_stages, uint32_t tmem, int t) {
+    const uint32_t lane_base = (uint32_t)((t >> 5) * 32) << 16;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x, ++g) {
+        const Unit u = unit_of(p, unit);
+        const uint32_t slot = g % kStages, buf = g & 1u;
+        ok = __all_sync(0xffffffffu, wait_bar(sm, kBarFull + (int)slot, (g / kStages) & 1u, p, kWhereFull));
+        if (!ok) break;
+        // |q| of row t: its 16 chunks of 16 bytes, in any order (the sum does
+        // not care about the swizzle), from a lane-dependent start
+        const uint8_t *qrow = smem_stages + (size_t)slot * kStageBytes + kOffQ + t * 128;
+        float ss = 0.f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const int pos = (q + t) & 15;
+            const uint4 c = *reinterpret_cast<const uint4 *>(qrow + (pos >> 3) * kBox + (pos & 7) * 16);
+            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(h2[e]);
+                ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+            }
+        }
+        ptx::mbar_arrive(sm.b(kBarEmpty + (int)slot));
+        const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+        ok = __all_sync(0xffffffffu, wait_bar(sm, kBarAccFull + (int)buf, (g >> 1) & 1u, p, kWhereAccFull));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const int row = u.row0 + t;
+        const bool row_ok = row < u.row_end;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(row_ok ? row : 0) * (size_t)p.ld + (size_t)u.head * 128);
+#pragma unroll 1
+        for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(tmem + lane_base + 128u * buf + 32u * (uint32_t)c4, r);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence(r);
+            if (row_ok) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
+                    dst[c4 * 4 + v] = w;
+                }
+            }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(sm.b(kBarAccEmpty + (int)buf));
+    }
+}
+
+}  // namespace ro
+
+// W = S_fwd[p] + S_rev[n] of chunk blockIdx.x, head blockIdx.y, as bf16 hi + lo.
+__global__ void __launch_bounds__(256)
+    vda_wsplit_kernel(const float *__restrict__ states, int frames, int chunk_frames, int window_chunks,
+                      __nv_bfloat16 *__restrict__ wsplit) {
+    const int c = (int)blockIdx.x, h = (int)blockIdx.y;
+    const int H = (int)gridDim.y, chunks = (int)gridDim.x;
+    const int p = max((c - window_chunks) * chunk_frames - 1, 0);
+    const int nx = min((c + window_chunks + 1) * chunk_frames, frames - 1);
+    const float4 *sf = reinterpret_cast<const float4 *>(states + ((size_t)h * frames + p) * kD * kD);
+    const float4 *sr = reinterpret_cast<const float4 *>(states + (((size_t)H + h) * frames + nx) * kD * kD);
+    __nv_bfloat16 *hi = wsplit + ((size_t)h * chunks + c) * 2 * kD * kD;
+    __nv_bfloat16 *lo = hi + kD * kD;
+    for (int e = (int)threadIdx.x; e < kD * kD / 4; e += (int)blockDim.x) {
+        const float4 a = sf[e], b = sr[e];
+        const float w[4] = {a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w};
+        __nv_bfloat16 wh[4], wl[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split_bf16(w[i], wh[i], wl[i]);
+        *reinterpret_cast<uint2 *>(hi + 4 * e) = *reinterpret_cast<const uint2 *>(wh);
+        *reinterpret_cast<uint2 *>(lo + 4 * e) = *reinterpret_cast<const uint2 *>(wl);
+    }
+}
+
+__global__ void __launch_bounds__(ro::kThreads, 1)
+    vda_readout_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_w,
+                          const ro::Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    ro::Smem sm;
+    sm.stages = base;
+    sm.bar = base + ro::kSmemBar;
+    sm.abort_flag = reinterpret_cast<volatile int *>(smem + ro::kSmemMisc + 4);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + ro::kSmemMisc);
+    const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ro::kStages; ++s) {
+            ptx::mbar_init(sm.b(ro::kBarFull + s), 1);
+            ptx::mbar_init(sm.b(ro::kBarEmpty + s), 1 + 128);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(sm.b(ro::kBarAccFull + b), 1);
+            ptx::mbar_init(sm.b(ro::kBarAccEmpty + b), 128);
+        }
+        ptx::mbar_init(sm.b(ro::kBarDrain), 1);
+        *sm.abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == ro::kTmaWarp && lane == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_w);
+    }
+    if (warp == ro::kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), ro::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
+    if (warp == ro::kTmaWarp) {
+        if (lane == 0) ro::producer(&tm_q, &tm_w, p, sm);
+    } else if (warp == ro::kMmaWarp) {
+        if (lane == 0) ro::mma_issuer(p, sm, tmem);
+    } else {
+        ro::epilogue(p, sm, smem, tmem, (int)threadIdx.x);
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == ro::kMmaWarp) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, ro::kTmemCols);
+    }
+}
+
+// [n, ld] bf16 row-major, boxes of box_rows rows x 64 columns, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t n, int ld, int box_rows) {
     EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)n};
     const cuuint64_t strides[1] = {(cuuint64_t)ld * 2u};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)kTok};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1u, 1u};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -365,7 +633,7 @@ fv_status launch_vda_stats_tc(const DeltaLaunch &a, float *ws_m, float *ws_c, cu
     if (frames <= 2) return FV_OK;
     const int ld = a.heads * kD;
     CUtensorMap mk, mv;
-    if (!make_map(&mk, a.k, a.n, ld) || !make_map(&mv, a.v, a.n, ld)) return FV_ERR_LAUNCH;
+    if (!make_map(&mk, a.k, a.n, ld, kTok) || !make_map(&mv, a.v, a.n, ld, kTok)) return FV_ERR_LAUNCH;
     Params p;
     p.beta = a.beta;
     p.ws_m = ws_m;
@@ -379,6 +647,46 @@ fv_status launch_vda_stats_tc(const DeltaLaunch &a, float *ws_m, float *ws_c, cu
     p.num_units = (frames - 2) * a.heads;
     const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
     vda_stats_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
+}
+
+fv_status launch_vda_readout_tc(const DeltaLaunch &a, __nv_bfloat16 *wsplit, cudaStream_t stream) {
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FV_ERR_LAUNCH;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(vda_readout_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     ro::kSmemBytes) != cudaSuccess)
+                return FV_ERR_LAUNCH;
+            attr_set[dev] = true;
+        }
+    }
+    const int frames = (int)(a.n / a.frame_tokens);
+    const int chunks = (frames + a.chunk_frames - 1) / a.chunk_frames;
+    const int ld = a.heads * kD;
+    vda_wsplit_kernel<<<dim3(chunks, a.heads), 256, 0, stream>>>(a.states, frames, a.chunk_frames, a.window_chunks,
+                                                                 wsplit);
+    CUtensorMap mq, mw;
+    if (!make_map(&mq, a.q, a.n, ld, ro::kRows) ||
+        !make_map(&mw, wsplit, (int64_t)a.heads * chunks * 2 * kD, kD, ro::kRows))
+        return FV_ERR_LAUNCH;
+    ro::Params p;
+    p.o = static_cast<__nv_bfloat16 *>(a.o);
+    p.status = a.status;
+    p.n = (int)a.n;
+    p.ld = ld;
+    p.heads = a.heads;
+    p.chunk_tokens = a.chunk_frames * a.frame_tokens;
+    p.chunks = chunks;
+    p.tiles_per_chunk = (p.chunk_tokens + ro::kRows - 1) / ro::kRows;
+    // every chunk but the last holds chunk_tokens rows; the last one's extra
+    // tiles (past the sequence) are still dealt out and store nothing
+    p.num_units = chunks * p.tiles_per_chunk * a.heads;
+    const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
+    vda_readout_tc_kernel<<<grid, ro::kThreads, ro::kSmemBytes, stream>>>(mq, mw, p);
     return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
 }
 

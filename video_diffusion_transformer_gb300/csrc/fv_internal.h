@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -74,6 +75,9 @@ struct DeltaLaunch {
 // The per-frame sums I + A_t -> ws_m and B_t -> ws_c of frames 1 .. F-2 on the
 // tensor cores (layout [heads, frames, 128, 128]).
 fv_status launch_vda_stats_tc(const DeltaLaunch &a, float *ws_m, float *ws_c, cudaStream_t stream);
+// o = (S_fwd[p] + S_rev[n]) q / |q| for every token, on the tensor cores;
+// wsplit: scratch of heads * chunks * 2 * 128 * 128 bf16.
+fv_status launch_vda_readout_tc(const DeltaLaunch &a, __nv_bfloat16 *wsplit, cudaStream_t stream);
 
 // Enqueue the Video Delta Attention kernels (stats, solve, scan, readout).
 fv_status launch_delta_attn(const DeltaLaunch &a, cudaStream_t stream);
