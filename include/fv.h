@@ -179,6 +179,9 @@ fv_status fv_delta_attn(const void *Q, const void *K, const void *V, const float
  *               every query tile, ascending.
  * workspace:    device scratch of at least fv_vsa_workspace_bytes(...) bytes
  *               (256-byte aligned), caller-owned; workspace_bytes is its size.
+ *               It holds the tile means, the kept-tile lists and a tile-major
+ *               copy of K and V (2 x H x tiles x 16 KB: 2.2 GB at 72 x 24 x 42
+ *               with 56 heads).
  * lse:          nullable device float32 [H, N], as fv_attn_fwd.
  * Errors: FV_ERR_NULL, FV_ERR_SHAPE (grid, N, topk, tile count, D, H),
  * FV_ERR_ALIGN (16-byte Q/K/V/O, 4-byte selected and lse, 256-byte

@@ -117,38 +117,54 @@ __device__ __forceinline__ uint64_t tile_token_mask(const Geo &g, int tile) {
 }
 
 // ----------------------------------------------------------------- pool
-// Means of q and k of every head over the tokens of tile blockIdx.x: thread
-// handles 8 channels (16 bytes) at a time, tokens in the tile's raster order.
+// Tile blockIdx.x: the means of q and k of every head over the tile's tokens,
+// and a tile-major copy of K and V for the fine kernel.  Thread handles 8
+// channels (16 bytes) of every head-row at a time, the tile's 64 box rows in
+// raster order (rows outside the grid are copied as zeros).
+//
+// Copy layout: [heads, tiles, 2 channel halves, 64 rows, 64 channels] bf16,
+// each (tile, half) an 8 KB block already in the 128-byte swizzled order the
+// tensor core reads (16-byte chunk j of row r stored at chunk j ^ (r % 8)),
+// so the fine kernel fetches it with one contiguous bulk copy.
 __global__ void __launch_bounds__(256)
-    vsa_pool_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k, Geo g, int heads,
-                    float *__restrict__ qbar, float *__restrict__ kbar) {
+    vsa_pool_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                    const __nv_bfloat16 *__restrict__ v, Geo g, int heads, float *__restrict__ qbar,
+                    float *__restrict__ kbar, __nv_bfloat16 *__restrict__ kp, __nv_bfloat16 *__restrict__ vp) {
     const int tile = (int)blockIdx.x;
     const TileCoord c = tile_coord(g, tile);
     const int nw = min(4, g.width - c.w0), nh = min(4, g.height - c.h0), nt = min(4, g.frames - c.t0);
     const int ld = heads * kD;
     const float count = (float)(nw * nh * nt);
     for (int ch = (int)threadIdx.x; ch < ld / 8; ch += (int)blockDim.x) {
+        const int h = (ch * 8) / kD, half = ((ch * 8) % kD) / 64, j = ch & 7;
+        const size_t blk = (((size_t)h * g.num_tiles + tile) * 2 + half) * (size_t)(kTok * 64);
         float sq[8], sk[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) sq[e] = sk[e] = 0.f;
-        for (int lt = 0; lt < nt; ++lt)
-            for (int lh = 0; lh < nh; ++lh)
-                for (int lw = 0; lw < nw; ++lw) {
-                    const int64_t tok = ((int64_t)(c.t0 + lt) * g.height + (c.h0 + lh)) * g.width + (c.w0 + lw);
-                    const uint4 a = *reinterpret_cast<const uint4 *>(q + tok * ld + ch * 8);
-                    const uint4 b = *reinterpret_cast<const uint4 *>(k + tok * ld + ch * 8);
-                    const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
-                    const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
+        for (int r = 0; r < kTok; ++r) {
+            const int lt = r >> 4, lh = (r >> 2) & 3, lw = r & 3;
+            uint4 kk = make_uint4(0u, 0u, 0u, 0u), vv = make_uint4(0u, 0u, 0u, 0u);
+            if (lt < nt && lh < nh && lw < nw) {
+                const int64_t tok = ((int64_t)(c.t0 + lt) * g.height + (c.h0 + lh)) * g.width + (c.w0 + lw);
+                const uint4 a = *reinterpret_cast<const uint4 *>(q + tok * ld + ch * 8);
+                kk = *reinterpret_cast<const uint4 *>(k + tok * ld + ch * 8);
+                vv = *reinterpret_cast<const uint4 *>(v + tok * ld + ch * 8);
+                const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
+                const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&kk);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 fa = __bfloat1622float2(pa[e]), fb = __bfloat1622float2(pb[e]);
-                        sq[2 * e] += fa.x;
-                        sq[2 * e + 1] += fa.y;
-                        sk[2 * e] += fb.x;
-                        sk[2 * e + 1] += fb.y;
-                    }
+                for (int e = 0; e < 4; ++e) {
+                    const float2 fa = __bfloat1622float2(pa[e]), fb = __bfloat1622float2(pb[e]);
+                    sq[2 * e] += fa.x;
+                    sq[2 * e + 1] += fa.y;
+                    sk[2 * e] += fb.x;
+                    sk[2 * e + 1] += fb.y;
                 }
-        const int h = (ch * 8) / kD, d = (ch * 8) % kD;
+            }
+            const size_t off = blk + (size_t)r * 64 + (size_t)((j ^ (r & 7)) * 8);
+            *reinterpret_cast<uint4 *>(kp + off) = kk;
+            *reinterpret_cast<uint4 *>(vp + off) = vv;
+        }
+        const int d = (ch * 8) % kD;
         float *dq = qbar + ((size_t)h * g.num_tiles + tile) * kD + d;
         float *dk = kbar + ((size_t)h * g.num_tiles + tile) * kD + d;
 #pragma unroll
@@ -266,6 +282,8 @@ struct Params {
     int *status;
     const int32_t *lists;   // [heads, pairs, list_ld] union entries: tile | owner bits << 16
     const int32_t *counts;  // [heads, pairs]
+    const uint8_t *kp, *vp; // tile-major copies of K and V (8 KB per tile and channel half)
+    const uint8_t *zero;    // 8 KB of zeros, stands in for an absent tile
     Geo g;
     int n, ld, pairs, num_units, list_ld;
     float scale_log2;
@@ -306,6 +324,24 @@ __device__ __forceinline__ void load_tile(const CUtensorMap *map, const Params &
     const uint32_t d = dst + (uint32_t)(half * kBoxBytes);
     tma_load_4d(d, map, bar, x0, c.w0, c.h0, c.t0);
     tma_load_4d(d + kHalfBytes, map, bar, x0 + 64, c.w0, c.h0, c.t0);
+}
+
+// Both channel halves of kept tile `tile` of head `head` into rows
+// [64 half, 64 half + 64) of a 32 KB K or V operand tile: two 8 KB bulk copies
+// from the tile-major copy (an absent tile, index >= tiles, copies zeros).
+__device__ __forceinline__ void load_kv_tile(const uint8_t *src_base, const Params &p, uint32_t dst, int half,
+                                             int head, int tile, uint32_t bar) {
+    const uint32_t d = dst + (uint32_t)(half * kBoxBytes);
+    for (int c = 0; c < 2; ++c) {
+        const uint8_t *src = tile < p.g.num_tiles
+                                 ? src_base + (((size_t)head * p.g.num_tiles + tile) * 2 + c) * (size_t)kBoxBytes
+                                 : p.zero;
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                d + (uint32_t)(c * kHalfBytes)),
+            "l"(src), "n"(kBoxBytes), "r"(bar)
+            : "memory");
+    }
 }
 
 // A softmax warp's view of one unit's list: for batches of 32 entries, one
@@ -360,8 +396,7 @@ struct MaskWindow {
 };
 
 // One thread (lane 0 of the TMA warp) issues every copy.
-__device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv, const Params &p,
-                         const Smem &sm, int lane) {
+__device__ void producer(const CUtensorMap *tq, const Params &p, const Smem &sm, int lane) {
     if (lane != 0) return;
     uint32_t loads = 0, q_loads = 0;
     bool ok = true;
@@ -379,22 +414,22 @@ __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUt
         const int32_t *lst = p.lists + ((size_t)head * p.pairs + pr) * p.list_ld;
         const int cnt = p.counts[(size_t)head * p.pairs + pr];
         const int nkv = (cnt + 1) / 2;
-        auto load_kv = [&](const CUtensorMap *m, int j) -> bool {
+        auto load_kv = [&](const uint8_t *m, int j) -> bool {
             const uint32_t s = loads % kStages, ph = (loads / kStages) & 1u;
             if (!wait_bar(sm, kBarKvEmpty + (int)s, ph ^ 1u, p, kWhereKvEmpty)) return false;
             const int e0 = 2 * j < cnt ? lst[2 * j] : 0xFFFF, e1 = 2 * j + 1 < cnt ? lst[2 * j + 1] : 0xFFFF;
             ptx::mbar_arrive_expect_tx(sm.b(kBarKvFull + (int)s), kTileBytes);
             const uint32_t dst = sm.kv + s * (uint32_t)kTileBytes;
-            load_tile(m, p, dst, 0, e0 & 0xFFFF, x0, sm.b(kBarKvFull + (int)s));
-            load_tile(m, p, dst, 1, e1 & 0xFFFF, x0, sm.b(kBarKvFull + (int)s));
+            load_kv_tile(m, p, dst, 0, head, e0 & 0xFFFF, sm.b(kBarKvFull + (int)s));
+            load_kv_tile(m, p, dst, 1, head, e1 & 0xFFFF, sm.b(kBarKvFull + (int)s));
             ++loads;
             return true;
         };
-        ok = load_kv(tk, 0);
-        if (ok && nkv > 1) ok = load_kv(tk, 1);
+        ok = load_kv(p.kp, 0);
+        if (ok && nkv > 1) ok = load_kv(p.kp, 1);
         for (int j = 0; ok && j < nkv; ++j) {
-            ok = load_kv(tv, j);
-            if (ok && j + 2 < nkv) ok = load_kv(tk, j + 2);
+            ok = load_kv(p.vp, j);
+            if (ok && j + 2 < nkv) ok = load_kv(p.kp, j + 2);
         }
     }
     for (uint32_t s = 0; s < (uint32_t)kStages && s < loads; ++s) {
@@ -720,8 +755,7 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    vsa_fine_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+    vsa_fine_kernel(const __grid_constant__ CUtensorMap tm_q, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -756,8 +790,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == kTmaWarp && lane == 0) {
         ptx::prefetch_tensormap(&tm_q);
-        ptx::prefetch_tensormap(&tm_k);
-        ptx::prefetch_tensormap(&tm_v);
     }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
@@ -768,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
     if (warp == kTmaWarp) {
-        producer(&tm_q, &tm_k, &tm_v, p, sm, lane);
+        producer(&tm_q, p, sm, lane);
     } else if (warp == kMmaWarp) {
         if (lane == 0) mma_issuer(p, sm, tmem);
     } else {
@@ -813,7 +845,7 @@ Geo make_geo(int frames, int height, int width) {
 size_t align256(size_t x) { return (x + 255u) & ~(size_t)255u; }
 
 struct WsLayout {
-    size_t qbar, kbar, lists, counts, total;
+    size_t qbar, kbar, lists, counts, kp, vp, zero, total;
 };
 
 WsLayout ws_layout(int heads, const Geo &g, int topk) {
@@ -824,7 +856,11 @@ WsLayout ws_layout(int heads, const Geo &g, int topk) {
     w.kbar = means;
     w.lists = 2 * means;
     w.counts = w.lists + align256((size_t)heads * pairs * 2 * topk * sizeof(int32_t));
-    w.total = w.counts + align256((size_t)heads * pairs * sizeof(int32_t));
+    w.kp = w.counts + align256((size_t)heads * pairs * sizeof(int32_t));
+    const size_t copy = align256((size_t)heads * g.num_tiles * 2 * kBoxBytes);
+    w.vp = w.kp + copy;
+    w.zero = w.vp + copy;
+    w.total = w.zero + kBoxBytes;
     return w;
 }
 
@@ -865,12 +901,15 @@ fv_status launch_vsa_attn(const VsaLaunch &a, cudaStream_t stream) {
     float *kbar = reinterpret_cast<float *>(ws + w.kbar);
     int32_t *lists = reinterpret_cast<int32_t *>(ws + w.lists);
     int32_t *counts = reinterpret_cast<int32_t *>(ws + w.counts);
-    CUtensorMap mq, mk, mv;
-    if (!make_grid_map(&mq, a.q, g, ld) || !make_grid_map(&mk, a.k, g, ld) || !make_grid_map(&mv, a.v, g, ld))
-        return FV_ERR_LAUNCH;
+    CUtensorMap mq;
+    if (!make_grid_map(&mq, a.q, g, ld)) return FV_ERR_LAUNCH;
     const auto *q = static_cast<const __nv_bfloat16 *>(a.q);
     const auto *k = static_cast<const __nv_bfloat16 *>(a.k);
-    vsa_pool_kernel<<<g.num_tiles, 256, 0, stream>>>(q, k, g, a.heads, qbar, kbar);
+    const auto *v = static_cast<const __nv_bfloat16 *>(a.v);
+    if (cudaMemsetAsync(ws + w.zero, 0, kBoxBytes, stream) != cudaSuccess) return FV_ERR_LAUNCH;
+    vsa_pool_kernel<<<g.num_tiles, 256, 0, stream>>>(q, k, v, g, a.heads, qbar, kbar,
+                                                     reinterpret_cast<__nv_bfloat16 *>(ws + w.kp),
+                                                     reinterpret_cast<__nv_bfloat16 *>(ws + w.vp));
     vsa_select_kernel<<<dim3(pairs, a.heads), 256, (size_t)2 * g.num_tiles * 4, stream>>>(
         qbar, kbar, g, pairs, a.topk, a.selected, lists, counts);
     Params p;
@@ -879,6 +918,9 @@ fv_status launch_vsa_attn(const VsaLaunch &a, cudaStream_t stream) {
     p.status = a.status;
     p.lists = lists;
     p.counts = counts;
+    p.kp = ws + w.kp;
+    p.vp = ws + w.vp;
+    p.zero = ws + w.zero;
     p.g = g;
     p.n = (int)a.n;
     p.ld = ld;
@@ -887,7 +929,7 @@ fv_status launch_vsa_attn(const VsaLaunch &a, cudaStream_t stream) {
     p.list_ld = 2 * a.topk;
     p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
     const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
-    vsa_fine_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    vsa_fine_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, p);
     return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
 }
 
