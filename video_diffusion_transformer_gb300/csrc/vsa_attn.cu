@@ -196,83 +196,113 @@ __device__ uint32_t kth_largest_key(const uint32_t *keys, int n, int k, int lane
     return t;
 }
 
-// One CTA per (pair p, head): scores of query tiles 2p and 2p+1 against every
-// key tile, their top-k lists and the union list.
-__global__ void __launch_bounds__(256)
-    vsa_select_kernel(const float *__restrict__ qbar, const float *__restrict__ kbar, Geo g, int pairs, int topk,
-                      int32_t *__restrict__ selected, int32_t *__restrict__ lists, int32_t *__restrict__ counts) {
-    extern __shared__ uint32_t keys[];  // [2][num_tiles]
-    __shared__ uint32_t thr[2];
-    const int p = (int)blockIdx.x, h = (int)blockIdx.y;
+// One CTA per (group of up to 8 pairs of query tiles, head): the coarse
+// scores of the group's query tiles against every key tile (a thread scores
+// whole key tiles, the query means in shared memory), then per query tile the
+// top-k (one warp per row), then per pair the two ascending lists and their
+// union (one warp per pair).
+constexpr int kSelMaxRows = 16;
+constexpr int kSelSmemBytes = 200 * 1024;
+
+int select_pairs_per_cta(int num_tiles) {
+    const int floats = kSelSmemBytes / 4 - kSelMaxRows * kD;
+    const int rows = floats / num_tiles;
+    const int pairs = rows / 2;
+    return pairs < 1 ? 1 : (pairs > kSelMaxRows / 2 ? kSelMaxRows / 2 : pairs);
+}
+
+__global__ void __launch_bounds__(256, 1)
+    vsa_select_kernel(const float *__restrict__ qbar, const float *__restrict__ kbar, Geo g, int pairs,
+                      int pairs_per_cta, int topk, int32_t *__restrict__ selected, int32_t *__restrict__ lists,
+                      int32_t *__restrict__ counts) {
+    extern __shared__ uint32_t sh[];
+    float *qs = reinterpret_cast<float *>(sh);  // [kSelMaxRows][128] query means
+    uint32_t *keys = sh + kSelMaxRows * kD;     // [rows][num_tiles] score keys
+    __shared__ uint32_t thr[kSelMaxRows];
+    const int p0 = (int)blockIdx.x * pairs_per_cta, h = (int)blockIdx.y;
+    const int np = min(pairs_per_cta, pairs - p0);
     const int nt = g.num_tiles;
-    const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
-    const int r1 = 2 * p + 1 < nt ? 2 * p + 1 : 2 * p;  // a lone last tile scores twice, kept once
-    const float4 qa = reinterpret_cast<const float4 *>(qbar + ((size_t)h * nt + 2 * p) * kD)[lane];
-    const float4 qb = reinterpret_cast<const float4 *>(qbar + ((size_t)h * nt + r1) * kD)[lane];
-    for (int c = warp; c < nt; c += 8) {
-        const float4 kk = reinterpret_cast<const float4 *>(kbar + ((size_t)h * nt + c) * kD)[lane];
-        float sa = qa.x * kk.x + qa.y * kk.y + qa.z * kk.z + qa.w * kk.w;
-        float sb = qb.x * kk.x + qb.y * kk.y + qb.z * kk.z + qb.w * kk.w;
+    const int tid = (int)threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // rows past the group (or past the last tile) repeat the last tile; their
+    // scores are never used
+    for (int e = tid; e < kSelMaxRows * kD; e += (int)blockDim.x) {
+        const int tile = min(2 * p0 + e / kD, nt - 1);
+        qs[e] = qbar[((size_t)h * nt + tile) * kD + e % kD];
+    }
+    __syncthreads();
+    const int rows = 2 * np;
+    for (int c = tid; c < nt; c += (int)blockDim.x) {
+        const float4 *kr = reinterpret_cast<const float4 *>(kbar + ((size_t)h * nt + c) * kD);
+        float acc[kSelMaxRows];
+#pragma unroll
+        for (int r = 0; r < kSelMaxRows; ++r) acc[r] = 0.f;
+#pragma unroll 4
+        for (int d4 = 0; d4 < kD / 4; ++d4) {
+            const float4 kk = kr[d4];
+#pragma unroll
+            for (int r = 0; r < kSelMaxRows; ++r) {
+                const float4 qq = *reinterpret_cast<const float4 *>(qs + r * kD + 4 * d4);
+                acc[r] = fmaf(qq.x, kk.x, fmaf(qq.y, kk.y, fmaf(qq.z, kk.z, fmaf(qq.w, kk.w, acc[r]))));
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kSelMaxRows; ++r)
+            if (r < rows) keys[r * nt + c] = score_key(acc[r]);
+    }
+    __syncthreads();
+    for (int r = warp; r < rows; r += 8) {
+        const uint32_t t = kth_largest_key(keys + r * nt, nt, topk, lane);
+        if (lane == 0) thr[r] = t;
+    }
+    __syncthreads();
+    // One warp per pair walks the tiles in ascending order, 32 at a time: a
+    // tile is kept when its key beats the threshold, or equals it and enough
+    // lower tiles with the same key have not already filled the k slots.
+    const uint32_t below = (1u << lane) - 1u;
+    for (int pp = warp; pp < np; pp += 8) {
+        const int p = p0 + pp;
+        const uint32_t *ka_row = keys + (2 * pp) * nt, *kb_row = keys + (2 * pp + 1) * nt;
+        const bool has_b = 2 * p + 1 < nt;
+        const uint32_t ta = thr[2 * pp], tb = thr[2 * pp + 1];
+        int gt_a = 0, gt_b = 0;
+        for (int i = lane; i < nt; i += 32) {
+            gt_a += ka_row[i] > ta ? 1 : 0;
+            gt_b += kb_row[i] > tb ? 1 : 0;
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            sa += __shfl_xor_sync(0xffffffffu, sa, o);
-            sb += __shfl_xor_sync(0xffffffffu, sb, o);
+            gt_a += __shfl_xor_sync(0xffffffffu, gt_a, o);
+            gt_b += __shfl_xor_sync(0xffffffffu, gt_b, o);
         }
-        if (lane == 0) {
-            keys[c] = score_key(sa);
-            keys[nt + c] = score_key(sb);
+        const int eq_room_a = topk - gt_a, eq_room_b = topk - gt_b;
+        int eq_a = 0, eq_b = 0, na = 0, nb = 0, nu = 0;
+        int32_t *sel_a = selected + ((size_t)h * nt + 2 * p) * topk;
+        int32_t *sel_b = selected + ((size_t)h * nt + 2 * p + 1) * topk;
+        int32_t *uni = lists + ((size_t)h * pairs + p) * 2 * topk;
+        for (int base = 0; base < nt; base += 32) {
+            const int c = base + lane;
+            const bool in = c < nt;
+            const uint32_t ka = in ? ka_row[c] : 0u, kb = in ? kb_row[c] : 0u;
+            const uint32_t ea = __ballot_sync(0xffffffffu, in && ka == ta);
+            const uint32_t eb = __ballot_sync(0xffffffffu, in && kb == tb);
+            const bool keep_a = in && (ka > ta || (ka == ta && eq_a + __popc(ea & below) < eq_room_a));
+            const bool keep_b =
+                has_b && in && (kb > tb || (kb == tb && eq_b + __popc(eb & below) < eq_room_b));
+            const uint32_t ba = __ballot_sync(0xffffffffu, keep_a);
+            const uint32_t bb = __ballot_sync(0xffffffffu, keep_b);
+            const uint32_t bu = ba | bb;
+            if (keep_a) sel_a[na + __popc(ba & below)] = c;
+            if (keep_b) sel_b[nb + __popc(bb & below)] = c;
+            if (keep_a || keep_b)
+                uni[nu + __popc(bu & below)] = c | (keep_a ? 1 << 16 : 0) | (keep_b ? 1 << 17 : 0);
+            eq_a += __popc(ea);
+            eq_b += __popc(eb);
+            na += __popc(ba);
+            nb += __popc(bb);
+            nu += __popc(bu);
         }
+        if (lane == 0) counts[(size_t)h * pairs + p] = nu;
     }
-    __syncthreads();
-    if (warp < 2) {
-        const uint32_t t = kth_largest_key(keys + warp * nt, nt, topk, lane);
-        if (lane == 0) thr[warp] = t;
-    }
-    __syncthreads();
-    if (warp != 0) return;
-    // One warp walks the tiles in ascending order, 32 at a time: a tile is kept
-    // when its key beats the threshold, or equals it and enough lower tiles
-    // with the same key have not already filled the k slots.
-    const bool has_b = 2 * p + 1 < nt;
-    const uint32_t ta = thr[0], tb = thr[1];
-    int gt_a = 0, gt_b = 0;
-    for (int i = lane; i < nt; i += 32) {
-        gt_a += keys[i] > ta ? 1 : 0;
-        gt_b += keys[nt + i] > tb ? 1 : 0;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        gt_a += __shfl_xor_sync(0xffffffffu, gt_a, o);
-        gt_b += __shfl_xor_sync(0xffffffffu, gt_b, o);
-    }
-    const int eq_room_a = topk - gt_a, eq_room_b = topk - gt_b;
-    int eq_a = 0, eq_b = 0, na = 0, nb = 0, nu = 0;
-    int32_t *sel_a = selected + ((size_t)h * nt + 2 * p) * topk;
-    int32_t *sel_b = selected + ((size_t)h * nt + 2 * p + 1) * topk;
-    int32_t *uni = lists + ((size_t)h * pairs + p) * 2 * topk;
-    const uint32_t below = (1u << lane) - 1u;
-    for (int base = 0; base < nt; base += 32) {
-        const int c = base + lane;
-        const bool in = c < nt;
-        const uint32_t ka = in ? keys[c] : 0u, kb = in ? keys[nt + c] : 0u;
-        const uint32_t ea = __ballot_sync(0xffffffffu, in && ka == ta);
-        const uint32_t eb = __ballot_sync(0xffffffffu, in && kb == tb);
-        const bool keep_a = in && (ka > ta || (ka == ta && eq_a + __popc(ea & below) < eq_room_a));
-        const bool keep_b = has_b && in && (kb > tb || (kb == tb && eq_b + __popc(eb & below) < eq_room_b));
-        const uint32_t ba = __ballot_sync(0xffffffffu, keep_a);
-        const uint32_t bb = __ballot_sync(0xffffffffu, keep_b);
-        const uint32_t bu = ba | bb;
-        if (keep_a) sel_a[na + __popc(ba & below)] = c;
-        if (keep_b) sel_b[nb + __popc(bb & below)] = c;
-        if (keep_a || keep_b)
-            uni[nu + __popc(bu & below)] = c | (keep_a ? 1 << 16 : 0) | (keep_b ? 1 << 17 : 0);
-        eq_a += __popc(ea);
-        eq_b += __popc(eb);
-        na += __popc(ba);
-        nb += __popc(bb);
-        nu += __popc(bu);
-    }
-    if (lane == 0) counts[(size_t)h * pairs + p] = nu;
 }
 
 // ----------------------------------------------------------------- fine
@@ -887,7 +917,7 @@ fv_status launch_vsa_attn(const VsaLaunch &a, cudaStream_t stream) {
             if (cudaFuncSetAttribute(vsa_fine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
                     cudaSuccess ||
                 cudaFuncSetAttribute(vsa_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     2 * kMaxTiles * 4) != cudaSuccess)
+                                     kSelSmemBytes) != cudaSuccess)
                 return FV_ERR_LAUNCH;
             attr_set[dev] = true;
         }
@@ -910,8 +940,10 @@ fv_status launch_vsa_attn(const VsaLaunch &a, cudaStream_t stream) {
     vsa_pool_kernel<<<g.num_tiles, 256, 0, stream>>>(q, k, v, g, a.heads, qbar, kbar,
                                                      reinterpret_cast<__nv_bfloat16 *>(ws + w.kp),
                                                      reinterpret_cast<__nv_bfloat16 *>(ws + w.vp));
-    vsa_select_kernel<<<dim3(pairs, a.heads), 256, (size_t)2 * g.num_tiles * 4, stream>>>(
-        qbar, kbar, g, pairs, a.topk, a.selected, lists, counts);
+    const int ppc = select_pairs_per_cta(g.num_tiles);
+    const size_t sel_smem = ((size_t)kSelMaxRows * kD + (size_t)2 * ppc * g.num_tiles) * 4;
+    vsa_select_kernel<<<dim3((pairs + ppc - 1) / ppc, a.heads), 256, sel_smem, stream>>>(
+        qbar, kbar, g, pairs, ppc, a.topk, a.selected, lists, counts);
     Params p;
     p.o = static_cast<__nv_bfloat16 *>(a.o);
     p.lse = a.lse;
