@@ -146,8 +146,12 @@ fv_status fv_attn_fwd_window(const void *Q, const void *K, const void *V, void *
  * workspace:    device float32 [2, H, F, 128, 128], caller-owned scratch.
  * N = F * frame_tokens; F >= 1; chunk_frames >= 1; window_chunks >= 0; D = 128;
  * H 1 .. 256; all pointers 16-byte aligned; else FV_ERR_SHAPE / _NULL / _ALIGN.
- * Compute: float32 throughout (normalisation, sums, a Gauss-Jordan solve per frame,
- * the scans, the readout); O rounded once to bf16.
+ * Compute: the per-frame sums A_t, B_t and the readout run on the tensor cores
+ * with float32 accumulation; their scaled operands (beta-weighted normalised
+ * keys, values, the summed states) are split into bf16 hi + lo parts, so the
+ * products keep about float32 accuracy.  The per-frame solve (Gauss-Jordan on
+ * I + A_t, symmetric positive definite) and the scans run in float32.  O is
+ * rounded once to bf16.
  */
 fv_status fv_delta_attn(const void *Q, const void *K, const void *V, const float *beta,
                         const float *alpha, const float *text_state, int64_t N, int H, int D,
