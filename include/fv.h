@@ -8,6 +8,15 @@
  *   fv_attn_fwd         O = softmax(Q K^T * scale) V, full (unmasked), per head
  *   fv_gated_residual   out = x + gate[step] * a
  *
+ * and the attention variants the pages describe for the same tensors:
+ *
+ *   fv_attn_fwd_window  the windowed softmax branch of Video DeltaNet
+ *   fv_delta_attn       the linear (delta-rule) branch of Video DeltaNet
+ *   fv_vsa_attn         VSA-style block-sparse attention over 3D tiles
+ *   fv_adaln_modulate_tagged, fv_gated_residual_tagged
+ *                       the table row chosen per token (step and modality)
+ *   fv_attn_fwd_noalloc fv_attn_fwd for callers that cannot allocate
+ *
  * Sources ("FreeVideo: a 66 GB video transformer on an 8 GB card"):
  *   - section "What MiniMax H3 is, briefly": 56 heads of 128, Q/K/V 7168 wide,
  *     hidden size 5,376, tokens = latent frames x (H/32) x (W/32);
