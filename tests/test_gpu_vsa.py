@@ -142,3 +142,28 @@ def test_large_scores_late_in_the_list(hot_tile):
     idx = VS.tile_tokens(*grid)[hot_tile]
     k[idx] = (k[idx].float() * 16).to(torch.bfloat16)
     check(q, k, v, grid, fv.vsa_num_tiles(*grid))
+
+
+def test_fourteen_second_clip_grid_one_head():
+    """102 x 24 x 42 latent grid (the 14.4 s clip, 1,716 tiles), one head,
+    90% sparsity (172 kept); sampled rows."""
+    grid, heads = (102, 24, 42), 1
+    n = grid[0] * grid[1] * grid[2]
+    q, k, v = rand(n, heads, 102)
+    nt = fv.vsa_num_tiles(*grid)
+    topk = fv.vsa_topk(nt, 0.9)
+    assert (nt, topk) == (1716, 172)
+    rng = np.random.default_rng(2)
+    rows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 200)]))
+    check(q, k, v, grid, topk, rows=rows)
+
+
+def test_outlier_key_channels():
+    """1% of the key channels scaled by 20 (as in the half-resolution
+    workload): the coarse scores and the softmax both see the outliers."""
+    grid, heads = (8, 12, 16), 2
+    n = grid[0] * grid[1] * grid[2]
+    q, k, v = rand(n, heads, 21)
+    cols = torch.randperm(heads * 128, generator=torch.Generator().manual_seed(2))[: max(1, heads * 128 // 100)]
+    k[:, cols] = (k[:, cols].float() * 20).to(torch.bfloat16)
+    check(q, k, v, grid, fv.vsa_topk(fv.vsa_num_tiles(*grid), 0.75))
