@@ -169,6 +169,43 @@ __device__ __forceinline__ KvList kv_list(const Params &p, int qb) {
     return L;
 }
 
+// The i-th work unit of this CTA, as (head offset, q-block); false past the
+// last one.  Dense attention: units dealt round-robin, heads outermost (all
+// units cost the same).  Windowed attention: the q-blocks holding a row of
+// the first or the last frame see every key and cost several times more, so
+// they come first (one per CTA at most, for a launch of <= grid of them), the
+// others follow in their usual order, and the deal runs in snake order
+// (alternating direction every wave) so that the CTAs' totals even out.
+template <bool kWindow>
+__device__ __forceinline__ bool unit_at(const Params &p, int i, int &head_off, int &qb) {
+    const int grid = (int)gridDim.x, b = (int)blockIdx.x;
+    if (!kWindow) {
+        const int u = b + i * grid;
+        if (u >= p.num_units) return false;
+        head_off = u / p.q_blocks;
+        qb = u % p.q_blocks;
+        return true;
+    }
+    const int u = i * grid + ((i & 1) ? grid - 1 - b : b);
+    if (u >= p.num_units) return false;
+    const int heads = p.num_units / p.q_blocks;
+    const int T = p.frame_tokens, frames = frames_of(p);
+    const int a0 = min(p.q_blocks, (T + kUnitRows - 1) / kUnitRows);     // q-blocks touching frame 0
+    const int b1 = max(a0, ((frames - 1) * T) / kUnitRows);               // first q-block touching frame F-1
+    const int na = a0 + (p.q_blocks - b1);                                // anchor q-blocks per head
+    if (u < heads * na) {
+        head_off = u / na;
+        const int a = u % na;
+        qb = a < a0 ? a : b1 + (a - a0);
+    } else {
+        const int nn = p.q_blocks - na;
+        const int j = u - heads * na;
+        head_off = j / nn;
+        qb = a0 + j % nn;
+    }
+    return true;
+}
+
 struct Smem {
     uint32_t q, kv, bar;
     volatile int *abort_flag;
@@ -195,9 +232,9 @@ __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUt
     // wait runs out.  Such a load must not be waited for below.
     const int64_t skipped = blockIdx.x == 0 ? (int64_t)p.skip_load : -1;
     bool ok = true;
-    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
-        const int head = p.head_begin + unit / p.q_blocks;
-        const int qb = unit % p.q_blocks;
+    int head_off = 0, qb = 0;
+    for (int i = 0; ok && unit_at<kWindow>(p, i, head_off, qb); ++i) {
+        const int head = p.head_begin + head_off;
         const int x0 = head * kD;
         ok = wait_bar(sm, kBarQEmpty, (q_loads & 1u) ^ 1u, p, kWhereQEmpty);
         if (!ok) break;
@@ -280,10 +317,11 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
     uint32_t tile = 0;   // K/V tiles finished (same count for every q-tile)
     uint32_t units = 0;
     bool ok = true;
-    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
+    int head_off = 0, qb = 0;
+    for (int i = 0; ok && unit_at<kWindow>(p, i, head_off, qb); ++i) {
         ok = wait_bar(sm, kBarQFull, units & 1u, p, kWhereQFull);
         if (!ok) break;
-        const int n_kv = kv_list<kWindow>(p, unit % p.q_blocks).count;
+        const int n_kv = kv_list<kWindow>(p, qb).count;
         {
             const uint32_t s = ring % kStages;
             ok = wait_bar(sm, kBarKvFull + (int)s, (ring / kStages) & 1u, p, kWhereKvFull);
@@ -432,10 +470,11 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
     const uint32_t t_o = tmem + lane_base + 256u + (uint32_t)(128 * k);
     uint32_t tile = 0, units = 0;
     bool ok = true;
-    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
-        const int head = p.head_begin + unit / p.q_blocks;
-        const int row = (unit % p.q_blocks) * kUnitRows + k * kRows + t;
-        const KvList kl = kv_list<kWindow>(p, unit % p.q_blocks);
+    int head_off = 0, qb = 0;
+    for (int i = 0; ok && unit_at<kWindow>(p, i, head_off, qb); ++i) {
+        const int head = p.head_begin + head_off;
+        const int row = qb * kUnitRows + k * kRows + t;
+        const KvList kl = kv_list<kWindow>(p, qb);
         const int n_kv = kWindow ? kl.count : p.kv_tiles;
         RowWindow rw = {0, 0, true};
         int first_end = 0, last_begin = 0;
