@@ -397,6 +397,51 @@ def run_fv(args):
                    "effective_tflops": flops / (vms / 1e3) / 1e12,
                    "speedup_vs_dense": (sum(attn_ms) / len(attn_ms)) / vms}
 
+        # ---- the elementwise kernels alone, on the 14.4 s clip's 102,816 rows:
+        # L2 flushed (512 MB written) before every rep, 20 reps, median and best
+        elementwise = None
+        if not args.no_window:
+            rows = W.video_tokens(1344, 768, 345)
+            ge = torch.Generator(device=dev)
+            ge.manual_seed(4)
+            ex = torch.randn((rows, W.HIDDEN), generator=ge, device=dev).to(torch.bfloat16)
+            ea = torch.randn((rows, W.HIDDEN), generator=ge, device=dev).to(torch.bfloat16)
+            ey, eo = torch.empty_like(ex), torch.empty_like(ex)
+            flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+            hbm = peaks()["hbm_gbs"]
+
+            def time_reps(fn, reps=20):
+                fn()
+                times = []
+                for _ in range(reps):
+                    flush.fill_(1)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                    e1.synchronize()
+                    times.append(e0.elapsed_time(e1))
+                return statistics.median(times), min(times)
+
+            with torch.cuda.stream(stream):
+                mod = time_reps(lambda: fv.adaln_modulate(ex, shift, scale, W.ADALN_STEP, eps=EPS, out=ey,
+                                                          stream=stream))
+                gre = time_reps(lambda: fv.gated_residual(ex, ea, gate, W.ADALN_STEP, out=eo, stream=stream))
+            fv.sync_status(stream)
+            mod_bytes = rows * W.HIDDEN * 4 + 2 * W.HIDDEN * 4
+            gre_bytes = rows * W.HIDDEN * 6 + W.HIDDEN * 4
+
+            def entry(t, nbytes):
+                med, best = t
+                return {"median_ms": med, "best_ms": best, "bytes": nbytes, "gbs_median": nbytes / med / 1e6,
+                        "gbs_best": nbytes / best / 1e6,
+                        "frac_of_hbm_median": (nbytes / med / 1e6) / hbm if hbm else None}
+
+            elementwise = {"rows": rows, "hidden": W.HIDDEN, "flush": "512 MB written before every rep",
+                           "reps": 20, "peak_gbs": hbm, "adaln_modulate_bf16": entry(mod, mod_bytes),
+                           "gated_residual": entry(gre, gre_bytes)}
+            del ex, ea, ey, eo, flush
+
         # ---- end to end through the C ABI: pinned host inputs in, results out.
         # Every step copies its own inputs host->device and reads its results
         # back; copies run on their own streams, double-buffered, so step i's
@@ -469,7 +514,8 @@ def run_fv(args):
         cpu_baseline = {"value": fl / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                         "sample": f"{args.cpu_rows} query rows of each of the {w.heads} heads (of {w.n}) + "
                                   f"{args.cpu_rows} rows of modulate and gated residual; {dt:.1f} s",
-                        "parity_of_timed_output": sample_errors(o, outs)}
+                        "parity_of_timed_output": sample_errors(o, outs),
+                        "extrapolated_full_attention_s": w.flops / (fl / dt)}
 
     if rank != 0:
         return 0
@@ -502,6 +548,7 @@ def run_fv(args):
         "vdn_window_attention": window,
         "vdn_delta_attention": delta,
         "vsa_block_sparse_attention": vsa,
+        "elementwise_alone": elementwise,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -520,7 +567,8 @@ def parse(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=96, help="oracle query rows per head for cpu_baseline")
     ap.add_argument("--ref-rows", type=int, default=16, help="oracle query rows per head per reference step")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-window", action="store_true", help="skip the windowed-attention measurement")
+    ap.add_argument("--no-window", action="store_true",
+                    help="skip the side measurements (windowed, delta and VSA attention, elementwise kernels alone)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
