@@ -45,14 +45,8 @@ namespace {
 constexpr int kD = 128;
 constexpr int kTok = 64;                      // tokens of a tile
 constexpr int kRows = 128;                    // rows of a Q tile, keys of a K/V tile
-#ifndef VSA_KV_STAGES
-#define VSA_KV_STAGES 4
-#endif
-#ifndef VSA_Q_SLOTS
-#define VSA_Q_SLOTS 2
-#endif
-constexpr int kStages = VSA_KV_STAGES;        // K/V ring slots
-constexpr int kQSlots = VSA_Q_SLOTS;          // Q tiles in flight
+constexpr int kStages = 4;                    // K/V ring slots (5 or 6 measured no faster)
+constexpr int kQSlots = 2;                    // Q tiles in flight
 constexpr int kHalfBytes = kRows * 64 * 2;    // 128 rows x 64 channels (16 KB)
 constexpr int kTileBytes = 2 * kHalfBytes;    // 32 KB
 constexpr int kBoxBytes = kTok * 64 * 2;      // one tile x 64 channels (8 KB)
