@@ -16,7 +16,9 @@
 //               every key tile, the top-k of each of the two rows (a 32-step
 //               search for the k-th largest score, ties to the lower index),
 //               written as ascending tile lists, and the union of the two
-//               lists with one owner bit per query tile;
+//               lists with one owner bit per query tile, ordered so that a
+//               K/V tile pairs a tile of one list only with a tile of the
+//               other only (then the tiles both keep);
 //   vsa_fine    (persistent, one CTA per SM): unit = (head, pair).  A 128-row
 //               Q tile holds the pair's two query tiles (rows 0-63, 64-127),
 //               each brought in by one 4D TMA box {64 channels, 4, 4, 4}
@@ -50,14 +52,22 @@ constexpr int kQSlots = 2;                    // Q tiles in flight
 constexpr int kHalfBytes = kRows * 64 * 2;    // 128 rows x 64 channels (16 KB)
 constexpr int kTileBytes = 2 * kHalfBytes;    // 32 KB
 constexpr int kBoxBytes = kTok * 64 * 2;      // one tile x 64 channels (8 KB)
-constexpr int kThreads = 320;                 // warps 0-7 softmax, 8 TMA, 9 MMA
-constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kKeptBytes = 2 * kBoxBytes;     // one kept tile, both channel halves (16 KB)
+constexpr uint32_t kGroupBytes = 2048;        // 8 rows x both channel halves of a K/V operand tile
+constexpr int kThreads = 352;                 // warps 0-7 softmax, 8 TMA, 9-10 MMA
+constexpr int kTmaWarp = 8, kMmaWarp = 9;     // MMA warp 9 + g issues group g's work
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kMaxTiles = 16384;              // tile index fits the low 16 bits of a list entry
 
+// Load L of the K/V ring goes to slot L % kStages and completes on full
+// barrier L % (2 kStages): with two MMA threads taking loads out of order a
+// thread may wait on its load while the slot's previous use is still pending,
+// and a period of twice the slot count keeps that wait from matching an older
+// phase (see mma_issuer).
+constexpr int kKvFullBars = 2 * kStages;
 constexpr int kBarKvFull = 0;
-constexpr int kBarKvEmpty = kBarKvFull + kStages;
+constexpr int kBarKvEmpty = kBarKvFull + kKvFullBars;
 constexpr int kBarQFull = kBarKvEmpty + kStages;
 constexpr int kBarQEmpty = kBarQFull + kQSlots;
 constexpr int kBarSFull = kBarQEmpty + kQSlots;
@@ -65,8 +75,8 @@ constexpr int kBarPFull = kBarSFull + 2;
 constexpr int kBarOFull = kBarPFull + 2;
 constexpr int kBarMlReady = kBarOFull + 2;
 constexpr int kBarMerged = kBarMlReady + 1;
-constexpr int kBarDrain = kBarMerged + 1;
-constexpr int kNumBars = kBarDrain + 1;
+constexpr int kBarDrain = kBarMerged + 1;     // one per MMA issuer
+constexpr int kNumBars = kBarDrain + 2;
 
 constexpr int kSmemQ = 0;
 constexpr int kSmemKV = kSmemQ + kQSlots * kTileBytes;
@@ -116,10 +126,11 @@ __device__ __forceinline__ uint64_t tile_token_mask(const Geo &g, int tile) {
 // channels (16 bytes) of every head-row at a time, the tile's 64 box rows in
 // raster order (rows outside the grid are copied as zeros).
 //
-// Copy layout: [heads, tiles, 2 channel halves, 64 rows, 64 channels] bf16,
-// each (tile, half) an 8 KB block already in the 128-byte swizzled order the
-// tensor core reads (16-byte chunk j of row r stored at chunk j ^ (r % 8)),
-// so the fine kernel fetches it with one contiguous bulk copy.
+// Copy layout: [heads, tiles, 8 row groups, 2 channel halves, 8 rows,
+// 64 channels] bf16: each tile one contiguous 16 KB block, already in the
+// 128-byte swizzled order the tensor core reads (16-byte chunk j of row r
+// stored at chunk j ^ (r % 8)), so the fine kernel fetches a kept tile with
+// one bulk copy and its operand descriptors step 2 KB per 8 rows.
 __global__ void __launch_bounds__(256)
     vsa_pool_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                     const __nv_bfloat16 *__restrict__ v, Geo g, int heads, float *__restrict__ qbar,
@@ -131,7 +142,7 @@ __global__ void __launch_bounds__(256)
     const float count = (float)(nw * nh * nt);
     for (int ch = (int)threadIdx.x; ch < ld / 8; ch += (int)blockDim.x) {
         const int h = (ch * 8) / kD, half = ((ch * 8) % kD) / 64, j = ch & 7;
-        const size_t blk = (((size_t)h * g.num_tiles + tile) * 2 + half) * (size_t)(kTok * 64);
+        const size_t blk = ((size_t)h * g.num_tiles + tile) * (size_t)(kKeptBytes / 2) + (size_t)half * 512;
         float sq[8], sk[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) sq[e] = sk[e] = 0.f;
@@ -154,7 +165,7 @@ __global__ void __launch_bounds__(256)
                     sk[2 * e + 1] += fb.y;
                 }
             }
-            const size_t off = blk + (size_t)r * 64 + (size_t)((j ^ (r & 7)) * 8);
+            const size_t off = blk + (size_t)(r >> 3) * 1024 + (size_t)(r & 7) * 64 + (size_t)((j ^ (r & 7)) * 8);
             *reinterpret_cast<uint4 *>(kp + off) = kk;
             *reinterpret_cast<uint4 *>(vp + off) = vv;
         }
@@ -252,6 +263,11 @@ __global__ void __launch_bounds__(256, 1)
     // One warp per pair walks the tiles in ascending order, 32 at a time: a
     // tile is kept when its key beats the threshold, or equals it and enough
     // lower tiles with the same key have not already filled the k slots.
+    // The union is written so that K/V tile j (entries 2j, 2j+1) pairs a tile
+    // only query tile a keeps with one only b keeps: every warp then has one
+    // 64-key half to work on per K/V tile instead of zero or two.  Order:
+    // a-only and b-only interleaved, the longer side's excess, then the tiles
+    // both keep, each group ascending.  Two passes: the first counts.
     const uint32_t below = (1u << lane) - 1u;
     for (int pp = warp; pp < np; pp += 8) {
         const int p = p0 + pp;
@@ -269,45 +285,81 @@ __global__ void __launch_bounds__(256, 1)
             gt_b += __shfl_xor_sync(0xffffffffu, gt_b, o);
         }
         const int eq_room_a = topk - gt_a, eq_room_b = topk - gt_b;
-        int eq_a = 0, eq_b = 0, na = 0, nb = 0, nu = 0;
-        int32_t *sel_a = selected + ((size_t)h * nt + 2 * p) * topk;
-        int32_t *sel_b = selected + ((size_t)h * nt + 2 * p + 1) * topk;
-        int32_t *uni = lists + ((size_t)h * pairs + p) * 2 * topk;
-        for (int base = 0; base < nt; base += 32) {
+        // keep flags of tile base + lane; eq_a, eq_b count the tiles below base
+        // whose key equals the threshold, and advance past this batch
+        auto keeps = [&](int base, int &eq_a, int &eq_b, bool &keep_a, bool &keep_b) {
             const int c = base + lane;
             const bool in = c < nt;
             const uint32_t ka = in ? ka_row[c] : 0u, kb = in ? kb_row[c] : 0u;
             const uint32_t ea = __ballot_sync(0xffffffffu, in && ka == ta);
             const uint32_t eb = __ballot_sync(0xffffffffu, in && kb == tb);
-            const bool keep_a = in && (ka > ta || (ka == ta && eq_a + __popc(ea & below) < eq_room_a));
-            const bool keep_b =
-                has_b && in && (kb > tb || (kb == tb && eq_b + __popc(eb & below) < eq_room_b));
-            const uint32_t ba = __ballot_sync(0xffffffffu, keep_a);
-            const uint32_t bb = __ballot_sync(0xffffffffu, keep_b);
-            const uint32_t bu = ba | bb;
-            if (keep_a) sel_a[na + __popc(ba & below)] = c;
-            if (keep_b) sel_b[nb + __popc(bb & below)] = c;
-            if (keep_a || keep_b)
-                uni[nu + __popc(bu & below)] = c | (keep_a ? 1 << 16 : 0) | (keep_b ? 1 << 17 : 0);
+            keep_a = in && (ka > ta || (ka == ta && eq_a + __popc(ea & below) < eq_room_a));
+            keep_b = has_b && in && (kb > tb || (kb == tb && eq_b + __popc(eb & below) < eq_room_b));
             eq_a += __popc(ea);
             eq_b += __popc(eb);
+        };
+        int only_a = 0, only_b = 0;
+        {
+            int eq_a = 0, eq_b = 0;
+            for (int base = 0; base < nt; base += 32) {
+                bool keep_a, keep_b;
+                keeps(base, eq_a, eq_b, keep_a, keep_b);
+                only_a += __popc(__ballot_sync(0xffffffffu, keep_a && !keep_b));
+                only_b += __popc(__ballot_sync(0xffffffffu, keep_b && !keep_a));
+            }
+        }
+        const int mn = min(only_a, only_b), mx = max(only_a, only_b);
+        int eq_a = 0, eq_b = 0, na = 0, nb = 0, ia = 0, ib = 0, is = 0;
+        int32_t *sel_a = selected + ((size_t)h * nt + 2 * p) * topk;
+        int32_t *sel_b = selected + ((size_t)h * nt + 2 * p + 1) * topk;
+        int32_t *uni = lists + ((size_t)h * pairs + p) * 2 * topk;
+        for (int base = 0; base < nt; base += 32) {
+            const int c = base + lane;
+            bool keep_a, keep_b;
+            keeps(base, eq_a, eq_b, keep_a, keep_b);
+            const uint32_t ba = __ballot_sync(0xffffffffu, keep_a);
+            const uint32_t bb = __ballot_sync(0xffffffffu, keep_b);
+            const uint32_t boa = __ballot_sync(0xffffffffu, keep_a && !keep_b);
+            const uint32_t bob = __ballot_sync(0xffffffffu, keep_b && !keep_a);
+            const uint32_t bs = ba & bb;
+            if (keep_a) sel_a[na + __popc(ba & below)] = c;
+            if (keep_b) sel_b[nb + __popc(bb & below)] = c;
+            int pos = -1;
+            if (keep_a && keep_b) {
+                pos = mn + mx + is + __popc(bs & below);
+            } else if (keep_a) {
+                const int i = ia + __popc(boa & below);
+                pos = i < mn ? 2 * i : mn + i;
+            } else if (keep_b) {
+                const int i = ib + __popc(bob & below);
+                pos = i < mn ? 2 * i + 1 : mn + i;
+            }
+            if (pos >= 0) uni[pos] = c | (keep_a ? 1 << 16 : 0) | (keep_b ? 1 << 17 : 0);
             na += __popc(ba);
             nb += __popc(bb);
-            nu += __popc(bu);
+            ia += __popc(boa);
+            ib += __popc(bob);
+            is += __popc(bs);
         }
+        const int nu = mn + mx + is;
         if (lane == 0) counts[(size_t)h * pairs + p] = nu;
     }
 }
 
 // ----------------------------------------------------------------- fine
+// K/V tiles of a unit with `cnt` union entries: two kept tiles per K/V tile,
+// at least two K/V tiles (an all-absent second one when the union has one or
+// two tiles) so that each MMA issuer has work in every unit.
+__device__ __forceinline__ int kv_tiles(int cnt) { return cnt > 2 ? (cnt + 1) / 2 : 2; }
+
 struct Params {
     __nv_bfloat16 *o;
     float *lse;
     int *status;
     const int32_t *lists;   // [heads, pairs, list_ld] union entries: tile | owner bits << 16
     const int32_t *counts;  // [heads, pairs]
-    const uint8_t *kp, *vp; // tile-major copies of K and V (8 KB per tile and channel half)
-    const uint8_t *zero;    // 8 KB of zeros, stands in for an absent tile
+    const uint8_t *kp, *vp; // tile-major copies of K and V (16 KB per tile)
+    const uint8_t *zero;    // 16 KB of zeros, stands in for an absent tile
     Geo g;
     int n, ld, pairs, num_units, list_ld;
     float scale_log2;
@@ -350,22 +402,19 @@ __device__ __forceinline__ void load_tile(const CUtensorMap *map, const Params &
     tma_load_4d(d + kHalfBytes, map, bar, x0 + 64, c.w0, c.h0, c.t0);
 }
 
-// Both channel halves of kept tile `tile` of head `head` into rows
-// [64 half, 64 half + 64) of a 32 KB K or V operand tile: two 8 KB bulk copies
-// from the tile-major copy (an absent tile, index >= tiles, copies zeros).
-__device__ __forceinline__ void load_kv_tile(const uint8_t *src_base, const Params &p, uint32_t dst, int half,
+// Kept tile `tile` of head `head` into rows [64 pos, 64 pos + 64) of a 32 KB
+// K or V operand tile (8-row groups 2 KB apart, both channel halves in each):
+// one 16 KB bulk copy from the tile-major copy (an absent tile, index >=
+// tiles, copies zeros).
+__device__ __forceinline__ void load_kv_tile(const uint8_t *src_base, const Params &p, uint32_t dst, int pos,
                                              int head, int tile, uint32_t bar) {
-    const uint32_t d = dst + (uint32_t)(half * kBoxBytes);
-    for (int c = 0; c < 2; ++c) {
-        const uint8_t *src = tile < p.g.num_tiles
-                                 ? src_base + (((size_t)head * p.g.num_tiles + tile) * 2 + c) * (size_t)kBoxBytes
-                                 : p.zero;
-        asm volatile(
-            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                d + (uint32_t)(c * kHalfBytes)),
-            "l"(src), "n"(kBoxBytes), "r"(bar)
-            : "memory");
-    }
+    const uint8_t *src =
+        tile < p.g.num_tiles ? src_base + ((size_t)head * p.g.num_tiles + tile) * (size_t)kKeptBytes : p.zero;
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst + (uint32_t)(pos * kKeptBytes)),
+        "l"(src), "n"(kKeptBytes), "r"(bar)
+        : "memory");
 }
 
 // A softmax warp's view of one unit's list: for batches of 32 entries, one
@@ -437,29 +486,29 @@ __device__ void producer(const CUtensorMap *tq, const Params &p, const Smem &sm,
         ++q_loads;
         const int32_t *lst = p.lists + ((size_t)head * p.pairs + pr) * p.list_ld;
         const int cnt = p.counts[(size_t)head * p.pairs + pr];
-        const int nkv = (cnt + 1) / 2;
+        const int nkv = kv_tiles(cnt);
         auto load_kv = [&](const uint8_t *m, int j) -> bool {
             const uint32_t s = loads % kStages, ph = (loads / kStages) & 1u;
             if (!wait_bar(sm, kBarKvEmpty + (int)s, ph ^ 1u, p, kWhereKvEmpty)) return false;
             const int e0 = 2 * j < cnt ? lst[2 * j] : 0xFFFF, e1 = 2 * j + 1 < cnt ? lst[2 * j + 1] : 0xFFFF;
-            ptx::mbar_arrive_expect_tx(sm.b(kBarKvFull + (int)s), kTileBytes);
+            const uint32_t full = sm.b(kBarKvFull + (int)(loads % kKvFullBars));
+            ptx::mbar_arrive_expect_tx(full, kTileBytes);
             const uint32_t dst = sm.kv + s * (uint32_t)kTileBytes;
-            load_kv_tile(m, p, dst, 0, head, e0 & 0xFFFF, sm.b(kBarKvFull + (int)s));
-            load_kv_tile(m, p, dst, 1, head, e1 & 0xFFFF, sm.b(kBarKvFull + (int)s));
+            load_kv_tile(m, p, dst, 0, head, e0 & 0xFFFF, full);
+            load_kv_tile(m, p, dst, 1, head, e1 & 0xFFFF, full);
             ++loads;
             return true;
         };
         ok = load_kv(p.kp, 0);
-        if (ok && nkv > 1) ok = load_kv(p.kp, 1);
+        if (ok) ok = load_kv(p.kp, 1);
         for (int j = 0; ok && j < nkv; ++j) {
             ok = load_kv(p.vp, j);
             if (ok && j + 2 < nkv) ok = load_kv(p.kp, j + 2);
         }
     }
-    for (uint32_t s = 0; s < (uint32_t)kStages && s < loads; ++s) {
-        const uint32_t last = ((loads - 1u - s) / kStages) * kStages + s;
-        drain_bar(sm, kBarKvFull + (int)s, (last / kStages) & 1u, p);
-    }
+    // the last kKvFullBars loads each hold their own full barrier
+    for (uint32_t l = loads > (uint32_t)kKvFullBars ? loads - kKvFullBars : 0u; l < loads; ++l)
+        drain_bar(sm, kBarKvFull + (int)(l % kKvFullBars), (l / kKvFullBars) & 1u, p);
     for (uint32_t i = 0; i < (uint32_t)kQSlots && i < q_loads; ++i) {
         const uint32_t last = q_loads - 1u - i;
         drain_bar(sm, kBarQFull + (int)(last % kQSlots), (last / kQSlots) & 1u, p);
@@ -468,34 +517,50 @@ __device__ void producer(const CUtensorMap *tq, const Params &p, const Smem &sm,
 
 constexpr uint64_t kDescTile = (uint64_t)(kTileBytes >> 4);
 
+// S = Q K^T: Q in the TMA layout (channel halves 16 KB apart, 8-row groups
+// 1 KB apart), K in the tile-major layout (halves 1 KB apart, groups 2 KB).
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
     constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
 #pragma unroll
     for (int kk = 0; kk < kD / 16; ++kk) {
-        const uint64_t off = (uint64_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
-        ptx::mma_ss(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
+        const uint64_t qoff = (uint64_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+        const uint64_t koff = (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
+        ptx::mma_ss(d_tmem, q_desc + qoff, k_desc + koff, idesc, kk > 0 ? 1u : 0u);
     }
 }
 
+// O += P V: V MN-major in the tile-major layout, 16 keys = two 2 KB groups.
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc, bool accumulate) {
     constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, true);
 #pragma unroll
     for (int kk = 0; kk < kRows / 16; ++kk) {
-        const uint64_t off = (uint64_t)((kk * 16 * 128) >> 4);
+        const uint64_t off = (uint64_t)((kk * 2 * kGroupBytes) >> 4);
         ptx::mma_ts(d_tmem, p_tmem + (uint32_t)(kk * 8), v_desc + off, idesc, (accumulate || kk > 0) ? 1u : 0u);
     }
 }
 
-__device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
+// Issuer of softmax group g's tensor work: S_g = Q K_j^T and O_g += P_g V_j
+// for the unit's K/V tiles j = g, g + 2, ...  Two threads (one per group, in
+// different warps) feed the tensor core, so one's waits and commits overlap
+// the other's MMAs.  Each finds its tiles' K/V ring slots from the
+// producer's fixed load order: K_0, K_1, then V_j, K_{j+2} for j = 0, 1, ...
+// A thread waits on load L only after its own previous load L' >= L - 4
+// completed (every unit has >= 2 K/V tiles, so each thread's loads are at
+// most 3 apart); L' was issued after every load <= L' - 4 had been consumed,
+// so load L - 8, the previous user of L's full barrier, is complete and the
+// parity wait cannot match a stale phase.
+__device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem, int g) {
     const uint64_t q0 = ptx::sdesc_sw128(sm.q, 16, 1024);
-    const uint64_t kv0 = ptx::sdesc_sw128(sm.kv, 16, 1024);
-    const uint64_t v0 = ptx::sdesc_sw128(sm.kv, kHalfBytes, 1024);
-    uint32_t idx = 0, uu = 0, ptile[2] = {0u, 0u};
+    const uint64_t kv0 = ptx::sdesc_sw128(sm.kv, 16, kGroupBytes);
+    const uint64_t v0 = ptx::sdesc_sw128(sm.kv, 1024, kGroupBytes);
+    const uint32_t t_s = tmem + 128u * (uint32_t)g, t_o = tmem + 256u + 128u * (uint32_t)g;
+    uint32_t base = 0, uu = 0, ptile = 0;  // loads of the CTA's earlier units, units, P tiles seen
     bool ok = true;
-    auto next_kv = [&](uint32_t &slot) -> bool {
-        slot = idx % kStages;
-        const bool r = wait_bar(sm, kBarKvFull + (int)slot, (idx / kStages) & 1u, p, kWhereKvFull);
-        ++idx;
+    // wait for ring load `ld` (unit-relative) and return its slot
+    auto kv_ready = [&](uint32_t ld, uint32_t &slot) -> bool {
+        const uint32_t L = base + ld;
+        slot = L % kStages;
+        const bool r = wait_bar(sm, kBarKvFull + (int)(L % kKvFullBars), (L / kKvFullBars) & 1u, p, kWhereKvFull);
         if (r) ptx::tc_fence_after();
         return r;
     };
@@ -506,51 +571,45 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
         if (!ok) break;
         ptx::tc_fence_after();
         const uint64_t qd = q0 + qs * kDescTile;
-        const int nkv = (p.counts[(size_t)head * p.pairs + pr] + 1) / 2;
+        const int nkv = kv_tiles(p.counts[(size_t)head * p.pairs + pr]);
+        const int m = nkv - 2;  // K_{j+2} is loaded for j < m
         uint32_t s;
-        ok = next_kv(s);
+        ok = kv_ready((uint32_t)g, s);  // K_g
         if (!ok) break;
-        issue_qk(tmem, qd, kv0 + s * kDescTile);
-        ptx::tc_commit(sm.b(kBarSFull));
+        issue_qk(t_s, qd, kv0 + s * kDescTile);
+        ptx::tc_commit(sm.b(kBarSFull + g));
         ptx::tc_commit(sm.b(kBarKvEmpty + (int)s));
-        if (nkv > 1) {
-            ok = next_kv(s);
-            if (!ok) break;
-            issue_qk(tmem + 128u, qd, kv0 + s * kDescTile);
-            ptx::tc_commit(sm.b(kBarSFull + 1));
-            ptx::tc_commit(sm.b(kBarKvEmpty + (int)s));
-        }
         // both groups must have read O_0 and O_1 of the previous unit
         if (uu > 0) {
             ok = wait_bar(sm, kBarMerged, (uu - 1u) & 1u, p, kWhereMerged);
             if (!ok) break;
             ptx::tc_fence_after();
         }
-        for (int j = 0; ok && j < nkv; ++j) {
-            const int k = j & 1;
-            ok = next_kv(s);
+        for (int j = g; ok && j < nkv; j += 2) {
+            const uint32_t lv = (uint32_t)(2 + j + (j < m ? j : m));  // V_j; K_{j+2} follows it
+            ok = kv_ready(lv, s);
             if (!ok) break;
-            ok = wait_bar(sm, kBarPFull + k, ptile[k] & 1u, p, kWherePFull);
+            ok = wait_bar(sm, kBarPFull + g, ptile & 1u, p, kWherePFull);
             if (!ok) break;
-            ++ptile[k];
+            ++ptile;
             ptx::tc_fence_after();
-            issue_pv(tmem + 256u + 128u * (uint32_t)k, tmem + 128u * (uint32_t)k, v0 + s * kDescTile, j >= 2);
+            issue_pv(t_o, t_s, v0 + s * kDescTile, j >= 2);
             ptx::tc_commit(sm.b(kBarKvEmpty + (int)s));
-            if (j + 2 >= nkv) ptx::tc_commit(sm.b(kBarOFull + k));
+            if (j + 2 >= nkv) ptx::tc_commit(sm.b(kBarOFull + g));
             if (j + 2 < nkv) {
-                ok = next_kv(s);
+                ok = kv_ready(lv + 1u, s);
                 if (!ok) break;
-                issue_qk(tmem + 128u * (uint32_t)k, qd, kv0 + s * kDescTile);
-                ptx::tc_commit(sm.b(kBarSFull + k));
+                issue_qk(t_s, qd, kv0 + s * kDescTile);
+                ptx::tc_commit(sm.b(kBarSFull + g));
                 ptx::tc_commit(sm.b(kBarKvEmpty + (int)s));
             }
         }
         if (!ok) break;
-        if (nkv == 1) ptx::tc_commit(sm.b(kBarOFull + 1));  // group 1 had no tile
         ptx::tc_commit(sm.b(kBarQEmpty + (int)qs));
+        base += 2u * (uint32_t)nkv;
     }
-    ptx::tc_commit(sm.b(kBarDrain));
-    drain_bar(sm, kBarDrain, 0u, p);
+    ptx::tc_commit(sm.b(kBarDrain + g));
+    drain_bar(sm, kBarDrain + g, 0u, p);
 }
 
 // -------------------------------------------------------------- softmax
@@ -637,7 +696,7 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
         const int head = unit / p.pairs, pr = unit % p.pairs;
         const int32_t *lst = p.lists + ((size_t)head * p.pairs + pr) * p.list_ld;
         const int cnt = p.counts[(size_t)head * p.pairs + pr];
-        const int nkv = (cnt + 1) / 2;
+        const int nkv = kv_tiles(cnt);
         MaskWindow win;
         win.init(lst, cnt, t & 31, qhalf, &p.g);
         float m_used = -INFINITY, l = 0.f;
@@ -793,13 +852,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + kSmemMisc);
     const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(sm.b(kBarKvFull + s), 1);
-            ptx::mbar_init(sm.b(kBarKvEmpty + s), 1);
-        }
+        for (int s = 0; s < kKvFullBars; ++s) ptx::mbar_init(sm.b(kBarKvFull + s), 1);
+        for (int s = 0; s < kStages; ++s) ptx::mbar_init(sm.b(kBarKvEmpty + s), 1);
         for (int k = 0; k < kQSlots; ++k) {
             ptx::mbar_init(sm.b(kBarQFull + k), 1);
-            ptx::mbar_init(sm.b(kBarQEmpty + k), 1);
+            ptx::mbar_init(sm.b(kBarQEmpty + k), 2);
         }
         for (int k = 0; k < 2; ++k) {
             ptx::mbar_init(sm.b(kBarSFull + k), 1);
@@ -809,6 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(sm.b(kBarMlReady), 256);
         ptx::mbar_init(sm.b(kBarMerged), 256);
         ptx::mbar_init(sm.b(kBarDrain), 1);
+        ptx::mbar_init(sm.b(kBarDrain + 1), 1);
         *sm.abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -825,8 +883,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
     if (warp == kTmaWarp) {
         producer(&tm_q, p, sm, lane);
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) mma_issuer(p, sm, tmem);
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        if (lane == 0) mma_issuer(p, sm, tmem, warp - kMmaWarp);
     } else {
         softmax_role(p, sm, tmem, warp >> 2, (int)threadIdx.x & 127);
     }
@@ -881,10 +939,10 @@ WsLayout ws_layout(int heads, const Geo &g, int topk) {
     w.lists = 2 * means;
     w.counts = w.lists + align256((size_t)heads * pairs * 2 * topk * sizeof(int32_t));
     w.kp = w.counts + align256((size_t)heads * pairs * sizeof(int32_t));
-    const size_t copy = align256((size_t)heads * g.num_tiles * 2 * kBoxBytes);
+    const size_t copy = align256((size_t)heads * g.num_tiles * kKeptBytes);
     w.vp = w.kp + copy;
     w.zero = w.vp + copy;
-    w.total = w.zero + kBoxBytes;
+    w.total = w.zero + kKeptBytes;
     return w;
 }
 
@@ -930,7 +988,7 @@ fv_status launch_vsa_attn(const VsaLaunch &a, cudaStream_t stream) {
     const auto *q = static_cast<const __nv_bfloat16 *>(a.q);
     const auto *k = static_cast<const __nv_bfloat16 *>(a.k);
     const auto *v = static_cast<const __nv_bfloat16 *>(a.v);
-    if (cudaMemsetAsync(ws + w.zero, 0, kBoxBytes, stream) != cudaSuccess) return FV_ERR_LAUNCH;
+    if (cudaMemsetAsync(ws + w.zero, 0, kKeptBytes, stream) != cudaSuccess) return FV_ERR_LAUNCH;
     vsa_pool_kernel<<<g.num_tiles, 256, 0, stream>>>(q, k, v, g, a.heads, qbar, kbar,
                                                      reinterpret_cast<__nv_bfloat16 *>(ws + w.kp),
                                                      reinterpret_cast<__nv_bfloat16 *>(ws + w.vp));
