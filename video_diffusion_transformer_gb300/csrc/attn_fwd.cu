@@ -56,7 +56,7 @@ constexpr int kTmaWarp = kSoftmaxWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + 1;
 constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;    // log2 units
+constexpr float kRedoSum = 1048576.0f;         // 2^20: largest tile sum kept against the reference max
 
 // barrier indices
 constexpr int kBarKvFull = 0;
@@ -524,20 +524,42 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
                                   (!kWindow || cm.all || (cm.w0 <= 0 && cm.w1 >= kRows) || cm.a0 >= kRows || cm.a1 <= 0);
             // one code path per warp: the tcgen05 copies are warp-collective
             const bool masked = __any_sync(0xffffffffu, !row_full && !row_none);
-            float m_tile = (masked ? row_max<true, kWindow>(s, cm) : row_max<false, kWindow>(s, cm)) * p.scale_log2;
-            if (kWindow && row_none) m_tile = -INFINITY;
+            // The reference maximum m_used is the first tile's row maximum; later
+            // tiles exponentiate against it directly (no per-tile maximum on the
+            // critical path) and only a tile whose probabilities sum above 2^20
+            // -- a score far above every earlier one -- takes its own maximum,
+            // rescales, and is exponentiated again.  So every p <= 2^20, l and
+            // O stay far inside float range, and the result is the softmax for
+            // any reference point.
             float factor = 1.f;
             bool rescale = false;
+            float tile_sum;
             if (j == 0) {
-                m_used = m_tile;
-            } else if (m_tile > m_used + kRescaleThreshold) {
-                factor = ptx::ex2_approx(m_used - m_tile);
-                m_used = m_tile;
-                rescale = true;
+                m_used = (masked ? row_max<true, kWindow>(s, cm) : row_max<false, kWindow>(s, cm)) * p.scale_log2;
+                if (kWindow && row_none) m_used = -INFINITY;
+                const float m_eff = (kWindow && row_none) ? INFINITY : m_used;
+                tile_sum = masked ? write_probs<true, kWindow>(s, cm, p.scale_log2, m_eff, t_s)
+                                  : write_probs<false, kWindow>(s, cm, p.scale_log2, m_eff, t_s);
+            } else {
+                const float m_eff = (kWindow && row_none) ? INFINITY : m_used;
+                tile_sum = masked ? write_probs<true, kWindow>(s, cm, p.scale_log2, m_eff, t_s)
+                                  : write_probs<false, kWindow>(s, cm, p.scale_log2, m_eff, t_s);
+                const bool redo = !(tile_sum <= kRedoSum);
+                if (__any_sync(0xffffffffu, redo)) {
+                    float m_tile =
+                        (masked ? row_max<true, kWindow>(s, cm) : row_max<false, kWindow>(s, cm)) * p.scale_log2;
+                    if (kWindow && row_none) m_tile = -INFINITY;
+                    if (m_tile > m_used) {
+                        factor = m_used == -INFINITY ? 0.f : ptx::ex2_approx(m_used - m_tile);
+                        m_used = m_tile;
+                        rescale = true;
+                    }
+                    const float m_new = (kWindow && row_none) ? INFINITY : m_used;
+                    ptx::tmem_st_wait();  // the first P is stored before it is overwritten
+                    tile_sum = masked ? write_probs<true, kWindow>(s, cm, p.scale_log2, m_new, t_s)
+                                      : write_probs<false, kWindow>(s, cm, p.scale_log2, m_new, t_s);
+                }
             }
-            const float m_eff = (kWindow && row_none) ? INFINITY : m_used;
-            const float tile_sum = masked ? write_probs<true, kWindow>(s, cm, p.scale_log2, m_eff, t_s)
-                                          : write_probs<false, kWindow>(s, cm, p.scale_log2, m_eff, t_s);
             l = l * factor + tile_sum;
             // O (complete through tile j-1, since S_j is) must carry the new maximum
             // before the next P.V accumulates into it.
