@@ -57,7 +57,7 @@ constexpr uint32_t kGroupBytes = 2048;        // 8 rows x both channel halves of
 constexpr int kThreads = 352;                 // warps 0-7 softmax, 8 TMA, 9-10 MMA
 constexpr int kTmaWarp = 8, kMmaWarp = 9;     // MMA warp 9 + g issues group g's work
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;
+constexpr float kRedoSum = 1048576.0f;        // 2^20: largest half sum kept against the reference max
 constexpr int kMaxTiles = 16384;              // tile index fits the low 16 bits of a list entry
 
 // Load L of the K/V ring goes to slot L % kStages and completes on full
@@ -728,9 +728,26 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
                 ptx::reg_fence(sc[0]);
                 ptx::reg_fence(sc[1]);
                 const bool full = (w[0] & w[1]) == 0xFFFFFFFFu;
+                // The row's first visible half sets the reference maximum m_used;
+                // later halves exponentiate against it directly and only a half
+                // whose probabilities sum above 2^20 takes its own maximum and is
+                // exponentiated again (the softmax does not depend on the
+                // reference point; every p stays <= 2^20).
+                float sum = 0.f;
+                bool need_max = __any_sync(0xffffffffu, m_used == -INFINITY);
+                if (!need_max) {
+                    sum = full ? half_probs<false>(sc, w, p.scale_log2, m_used, t_p)
+                               : half_probs<true>(sc, w, p.scale_log2, m_used, t_p);
+                    need_max = __any_sync(0xffffffffu, !(sum <= kRedoSum));
+                    if (need_max) ptx::tmem_st_wait();  // stored before it is overwritten
+                }
+                if (!need_max) {
+                    l += sum;
+                    continue;
+                }
                 const float mh = (full ? half_max<false>(sc, w) : half_max<true>(sc, w)) * p.scale_log2;
                 float f = 1.f;
-                if (mh > m_used + kRescaleThreshold) {
+                if (mh > m_used) {
                     if (m_used != -INFINITY) f = ptx::ex2_approx(m_used - mh);
                     m_used = mh;
                 }
