@@ -107,24 +107,28 @@ __global__ void __launch_bounds__(kDThreads, 1)
                 f[0] = c0.x, f[1] = c0.y, f[2] = c0.z, f[3] = c0.w;
                 f[4] = c1.x, f[5] = c1.y, f[6] = c1.z, f[7] = c1.w;
             }
-            // the pivot row divided by the pivot; its own column becomes 1 / pivot
+            // One update for every element: row i loses f_i times the pivot row
+            // divided by the pivot, with f_k - 1 for the pivot row itself (so it
+            // becomes the divided row), and the pivot column first set to the
+            // identity's column (so it becomes column k of the inverse:
+            // -f_i / pivot, and 1 / pivot on the diagonal).
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 rg[j] *= p;
                 rx[j] *= p;
             }
-            if (own_col) rg[kk] = p;
+            if (own_col) {
+                rg[kk] = p;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) g[i][kk] = (own_row && i == kk) ? 1.0f : 0.0f;
+            }
+            if (own_row) f[kk] -= 1.0f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const bool pivot_row = own_row && i == kk;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    float gij = g[i][j];
-                    if (j == kk && own_col) gij = 0.0f;
-                    const float ng = fmaf(-f[i], rg[j], gij);
-                    const float nx = fmaf(-f[i], rx[j], x[i][j]);
-                    g[i][j] = pivot_row ? rg[j] : ng;
-                    x[i][j] = pivot_row ? rx[j] : nx;
+                    g[i][j] = fmaf(-f[i], rg[j], g[i][j]);
+                    x[i][j] = fmaf(-f[i], rx[j], x[i][j]);
                 }
             }
         }
