@@ -189,7 +189,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    w = W.WORKLOADS[args.workload]
+    w = workload_of(args)
     inputs = cpu_inputs(w)
     rows = args.ref_rows
     times = []
@@ -212,6 +212,16 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def workload_of(args) -> W.Workload:
+    """The named workload, or (--heads) the same workload with fewer heads: a
+    small case of the same kernels for profiling."""
+    w = W.WORKLOADS[args.workload]
+    if args.heads is None:
+        return w
+    import dataclasses
+    return dataclasses.replace(w, heads=args.heads, head_group=min(w.head_group, args.heads))
 
 
 def config_of(w: W.Workload) -> dict:
@@ -247,7 +257,7 @@ def run_fv(args):
     import video_diffusion_transformer_gb300 as fv
     fv.load_library()
 
-    w = W.WORKLOADS[args.workload]
+    w = workload_of(args)
     cpu = cpu_inputs(w)
     q_h, k_h, v_h, xm_h, shift_h, scale_h, xr_h, a_h, gate_h = cpu
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
@@ -400,7 +410,7 @@ def run_fv(args):
         # ---- the elementwise kernels alone, on the 14.4 s clip's 102,816 rows:
         # L2 flushed (512 MB written) before every rep, 20 reps, median and best
         elementwise = None
-        if not args.no_window:
+        if not args.no_window and args.heads is None:
             rows = W.video_tokens(1344, 768, 345)
             ge = torch.Generator(device=dev)
             ge.manual_seed(4)
@@ -570,7 +580,12 @@ def parse(argv=None):
     ap.add_argument("--no-window", action="store_true",
                     help="skip the side measurements (windowed, delta and VSA attention, elementwise kernels alone)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="run the workload with this many heads (a small case of the same kernels, for "
+                         "profiling); the elementwise kernels are then not timed alone")
     args = ap.parse_args(argv)
+    if args.heads is not None and not 1 <= args.heads <= W.WORKLOADS[args.workload].heads:
+        ap.error("--heads must be between 1 and the workload's head count")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     return args
