@@ -15,9 +15,10 @@
 // Four kernels:
 //   stats   (frame, head; tensor cores, delta_tc.cu): I + A_t -> ws_m, B_t -> ws_c
 //   solve   (frame, head; float32): Gauss-Jordan on [I + A_t | B_t^T] in registers,
-//                          M'_t = Diag(alpha_t) (I + A_t)^{-1} -> ws_m,
-//                          C_t = B_t (I + A_t)^{-1} -> ws_c
-//   scan    (head, direction; float32): S <- S M'_t + C_t, frame by frame
+//                          M'_t = Diag(alpha_t) (I + A_t)^{-1} -> ws_m (bf16 hi/lo tiles),
+//                          C_t^T = (B_t (I + A_t)^{-1})^T -> ws_c
+//   scan    (head, direction; tensor cores, delta_tc.cu): S <- S M'_t + C_t,
+//           frame by frame, split-bf16 products with float32 accumulation
 //   readout (chunk rows, head; tensor cores, delta_tc.cu): o = (S_fwd[p] + S_rev[n]) q_hat,
 //           rounded to bf16
 // The scan is the only sequential part: 2 H chains of F - 2 128x128x128 steps.
@@ -46,8 +47,12 @@ constexpr size_t kMat = (size_t)kDv * kDv;
 // (ty, tx) holds rows ty*8 .. ty*8+7 and columns tx*8 .. tx*8+7 of both
 // halves.  Each step broadcasts the pivot row and pivot column through shared
 // memory (two alternating buffers, one barrier per step).
-// Written out: M' = Diag(alpha_t) M (the decay folded into the scan's
-// multiplier, S_{t-1} Diag(alpha_t) M = S_{t-1} M') and C.
+// Written out for the tensor-core scan: M' = Diag(alpha_t) M (the decay
+// folded into the scan's multiplier, S_{t-1} Diag(alpha_t) M = S_{t-1} M') as
+// two bf16 operand tiles, hi and lo (M' = hi + lo to 2^-17), each
+// [2 column halves][128 rows][64 columns] in the 128-byte swizzled layout
+// (16-byte chunk j of row q at chunk j ^ (q % 8)), in the frame's 64 KB of
+// ws_m; and C^T = X, float32 row-major, in ws_c.
 __global__ void __launch_bounds__(kDThreads, 1)
     vda_solve_kernel(const float *__restrict__ alpha, int frames, float *__restrict__ ws_m,
                      float *__restrict__ ws_c) {
@@ -134,133 +139,30 @@ __global__ void __launch_bounds__(kDThreads, 1)
         }
     }
     const float *al = alpha + ((size_t)h * frames + t) * kDv;
+    uint8_t *mo = reinterpret_cast<uint8_t *>(ws_m + base);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const float a = al[ty * 8 + i];
-        float4 *dst = reinterpret_cast<float4 *>(ws_m + base + (size_t)(ty * 8 + i) * kDv + tx * 8);
-        dst[0] = make_float4(a * g[i][0], a * g[i][1], a * g[i][2], a * g[i][3]);
-        dst[1] = make_float4(a * g[i][4], a * g[i][5], a * g[i][6], a * g[i][7]);
-    }
+        const int q = ty * 8 + i;
+        const float a = al[q];
+        uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {  // C[tx*8 + j][ty*8 + i] = X[ty*8 + i][tx*8 + j]
-        float4 *dst = reinterpret_cast<float4 *>(ws_c + base + (size_t)(tx * 8 + j) * kDv + ty * 8);
-        dst[0] = make_float4(x[0][j], x[1][j], x[2][j], x[3][j]);
-        dst[1] = make_float4(x[4][j], x[5][j], x[6][j], x[7][j]);
-    }
-}
-
-// ------------------------------------------------------------------- scan
-// One head, one direction: S <- S M'_t + C_t over the written frames, every
-// state stored.  The next frame's M' is copied into the other half of a
-// double buffer (cp.async) while the current step computes.  S is kept
-// transposed in shared memory with rows padded to kSLd floats, so both the
-// reads of a column of S and the transposed writes stay free of bank
-// conflicts.  Thread (ty, tx) computes rows {ty*4 + i, 64 + ty*4 + i} and
-// columns {tx*4 + j, 64 + tx*4 + j} of the product.
-constexpr int kSLd = kDv + 4;
-
-__device__ __forceinline__ void cp_async_16(float *dst, const float *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
-                 "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void scan_prefetch(float *dst, const float *src, int tid) {
-#pragma unroll
-    for (int e = 0; e < (int)(kMat / 4 / kDThreads); ++e) {
-        const int idx = (e * kDThreads + tid) * 4;
-        cp_async_16(dst + idx, src + idx);
-    }
-    cp_async_commit();
-}
-
-__global__ void __launch_bounds__(kDThreads, 1)
-    vda_scan_kernel(const float *__restrict__ text_state, int frames, const float *__restrict__ ws_m,
-                    const float *__restrict__ ws_c, float *__restrict__ states) {
-    extern __shared__ __align__(16) float sh[];
-    float *st = sh;                    // [kDv][kSLd]  S transposed
-    float *mb = sh + kDv * kSLd;       // [2][kDv][kDv] M' of this step and the next
-    const int h = (int)blockIdx.x;
-    const int dir = (int)blockIdx.y;  // 0 forward, 1 reverse
-    const int H = (int)gridDim.x;
-    const int tid = (int)threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    float *out = states + ((size_t)dir * H + h) * (size_t)frames * kMat;
-    const int steps = frames - 2;
-    auto frame_of = [&](int step) { return dir == 0 ? step : frames - 1 - step; };
-    if (steps >= 1) scan_prefetch(mb, ws_m + ((size_t)h * frames + frame_of(1)) * kMat, tid);
-    const int first = dir == 0 ? 0 : frames - 1;
-    for (int e = tid; e < (int)kMat; e += kDThreads) {
-        const float v = text_state != nullptr ? 0.5f * text_state[(size_t)h * kMat + e] : 0.0f;
-        st[(e % kDv) * kSLd + e / kDv] = v;
-        out[(size_t)first * kMat + e] = v;
-    }
-    int rows[8], cols[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        rows[i] = (i < 4 ? 0 : 64) + ty * 4 + (i & 3);
-        cols[i] = (i < 4 ? 0 : 64) + tx * 4 + (i & 3);
-    }
-    for (int step = 1; step <= steps; ++step) {
-        const int t = frame_of(step);
-        const size_t base = ((size_t)h * frames + t) * kMat;
-        const float *m = mb + (size_t)((step - 1) & 1) * kMat;
-        cp_async_wait_all();
-        __syncthreads();  // M'_t landed for every thread; the previous S is in st
-        if (step < steps)
-            scan_prefetch(mb + (size_t)(step & 1) * kMat, ws_m + ((size_t)h * frames + frame_of(step + 1)) * kMat,
-                          tid);
-        float cv[8][8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 *src = reinterpret_cast<const float4 *>(ws_c + base + (size_t)rows[i] * kDv);
-            const float4 c0 = src[tx], c1 = src[16 + tx];
-            cv[i][0] = c0.x, cv[i][1] = c0.y, cv[i][2] = c0.z, cv[i][3] = c0.w;
-            cv[i][4] = c1.x, cv[i][5] = c1.y, cv[i][6] = c1.z, cv[i][7] = c1.w;
+        for (int e = 0; e < 4; ++e) {
+            const float v0 = a * g[i][2 * e], v1 = a * g[i][2 * e + 1];
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(v0, v1);
+            const float2 hf = __bfloat1622float2(h2);
+            const __nv_bfloat162 l2 = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
+            hi[e] = *reinterpret_cast<const uint32_t *>(&h2);
+            lo[e] = *reinterpret_cast<const uint32_t *>(&l2);
         }
-        float acc[8][8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-#pragma unroll 4
-        for (int q = 0; q < kDv; ++q) {
-            const float4 s0 = *reinterpret_cast<const float4 *>(st + q * kSLd + ty * 4);
-            const float4 s1 = *reinterpret_cast<const float4 *>(st + q * kSLd + 64 + ty * 4);
-            const float4 m0 = *reinterpret_cast<const float4 *>(m + q * kDv + tx * 4);
-            const float4 m1 = *reinterpret_cast<const float4 *>(m + q * kDv + 64 + tx * 4);
-            const float si[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-            const float mj[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(si[i], mj[j], acc[i][j]);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] += cv[i][j];
-        __syncthreads();  // every read of the previous S is done
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float4 *dst = reinterpret_cast<float4 *>(out + (size_t)t * kMat + (size_t)rows[i] * kDv);
-            dst[tx] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-            dst[16 + tx] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            *reinterpret_cast<float4 *>(st + cols[j] * kSLd + ty * 4) =
-                make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
-            *reinterpret_cast<float4 *>(st + cols[j] * kSLd + 64 + ty * 4) =
-                make_float4(acc[4][j], acc[5][j], acc[6][j], acc[7][j]);
-        }
+        const size_t off = (size_t)(tx >> 3) * 16384 + (size_t)q * 128 + (size_t)(((tx & 7) ^ (q & 7)) << 4);
+        *reinterpret_cast<uint4 *>(mo + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(mo + 32768 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    __syncthreads();
-    // the far anchor frame writes nothing: it carries the last written state
-    if (frames >= 2) {
-        const int last = dir == 0 ? frames - 1 : 0;
-        for (int e = tid; e < (int)kMat; e += kDThreads) out[(size_t)last * kMat + e] = st[(e % kDv) * kSLd + e / kDv];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // C^T = X, row-major
+        float4 *dst = reinterpret_cast<float4 *>(ws_c + base + (size_t)(ty * 8 + i) * kDv + tx * 8);
+        dst[0] = make_float4(x[i][0], x[i][1], x[i][2], x[i][3]);
+        dst[1] = make_float4(x[i][4], x[i][5], x[i][6], x[i][7]);
     }
 }
 
@@ -268,10 +170,6 @@ __global__ void __launch_bounds__(kDThreads, 1)
 
 fv_status launch_delta_attn(const DeltaLaunch &a, cudaStream_t stream) {
     const int frames = (int)(a.n / a.frame_tokens);
-    const size_t scan_smem = (size_t)(kDv * kSLd + 2 * kDv * kDv) * sizeof(float);
-    if (cudaFuncSetAttribute(vda_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem) !=
-        cudaSuccess)
-        return FV_ERR_LAUNCH;
     float *ws_m = a.workspace;
     float *ws_c = a.workspace + (size_t)a.heads * frames * kMat;
     if (frames > 2) {
@@ -279,8 +177,8 @@ fv_status launch_delta_attn(const DeltaLaunch &a, cudaStream_t stream) {
         if (st != FV_OK) return st;
         vda_solve_kernel<<<dim3(frames - 2, a.heads), kDThreads, 0, stream>>>(a.alpha, frames, ws_m, ws_c);
     }
-    vda_scan_kernel<<<dim3(a.heads, 2), kDThreads, scan_smem, stream>>>(a.text_state, frames, ws_m, ws_c, a.states);
-    if (cudaGetLastError() != cudaSuccess) return FV_ERR_LAUNCH;
+    const fv_status st = launch_vda_scan_tc(a, ws_m, ws_c, stream);
+    if (st != FV_OK) return st;
     // the scan has consumed ws_m and ws_c: the readout's W splits reuse them
     return launch_vda_readout_tc(a, reinterpret_cast<__nv_bfloat16 *>(a.workspace), stream);
 }

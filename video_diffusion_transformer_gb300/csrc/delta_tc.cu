@@ -600,6 +600,264 @@ __global__ void __launch_bounds__(ro::kThreads, 1)
     }
 }
 
+// =================================================================== scan
+// One (head, direction) chain: S <- S M'_t + C_t frame by frame, every state
+// stored, on the tensor cores.  S_{t-1} lives in tensor memory as two bf16
+// operands (S = S_hi + S_lo to 2^-17); M'_t arrives from the solve as two bf16
+// operand tiles (hi, lo) already in the 128-byte swizzled MN-major layout;
+// D = S_hi M'_hi + S_hi M'_lo + S_lo M'_hi (24 MMAs, float32 accumulate; the
+// dropped S_lo M'_lo is below 2^-17 of the product).  C_t arrives transposed
+// (C^T, float32) so that thread r reads row r of C conflict-free.
+// 160 threads: warps 0-3 own the 128 state rows (TMEM lanes): they add C_t to
+// D, store S_t, and write its bf16 split for the next step; warp 4 (one
+// thread) loads M' (two buffers) and C (one buffer) by bulk copy and issues
+// the MMAs.
+namespace sc {
+
+constexpr int kThreads = 160;
+constexpr int kCtlWarp = 4;
+constexpr uint32_t kTmemCols = 256;            // D (0-127), S_hi (128-191), S_lo (192-255)
+constexpr int kMBytes = 2 * 32768;             // M'_t: hi and lo operand tiles
+constexpr int kCBytes = kD * kD * 4;           // C_t^T, float32
+constexpr int kSmemM = 0;                      // two buffers
+constexpr int kSmemC = kSmemM + 2 * kMBytes;
+constexpr int kBarM = 0;                       // two
+constexpr int kBarC = 2, kBarD = 3, kBarA = 4;
+constexpr int kNumBars = 5;
+constexpr int kSmemBar = kSmemC + kCBytes;
+constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
+constexpr int kSmemBytes = kSmemMisc + 16 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+constexpr int kWhereM = 1, kWhereC = 2, kWhereD = 3, kWhereA = 4, kWhereDrain = 5;
+
+struct Params {
+    const float *text_state;  // [heads, 128, 128] or null
+    const uint8_t *ws_m;      // per (head, frame): M'_t hi and lo tiles (64 KB)
+    const float *ws_c;        // per (head, frame): C_t^T
+    float *states;            // [2, heads, frames, 128, 128]
+    int *status;
+    int frames, heads;
+};
+
+struct Smem {
+    uint32_t m, c, bar;
+    const float *cf;  // the C buffer, generic address
+    volatile int *abort_flag;
+    __device__ uint32_t b(int i) const { return bar + 8u * (uint32_t)i; }
+};
+
+__device__ __forceinline__ bool wait_bar(const Smem &sm, int i, uint32_t parity, const Params &p, int where) {
+    return ptx::mbar_wait(sm.b(i), parity, sm.abort_flag, p.status, kDevTimeout | where);
+}
+
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 16384, [%2];" ::"r"(dst),
+                 "l"(src), "r"(bar)
+                 : "memory");
+}
+
+// 64 KB from src in four 16 KB copies, completing on barrier bar
+__device__ __forceinline__ void load64k(uint32_t dst, const uint8_t *src, uint32_t bar) {
+    ptx::mbar_arrive_expect_tx(bar, 65536u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) bulk_copy(dst + 16384u * (uint32_t)i, src + 16384 * i, bar);
+}
+
+__device__ __forceinline__ int frame_of(const Params &p, int dir, int step) {
+    return dir == 0 ? step : p.frames - 1 - step;
+}
+
+__device__ void control(const Params &p, const Smem &sm, uint32_t tmem, int h, int dir) {
+    const int steps = p.frames - 2;
+    auto mtile = [&](int step) { return p.ws_m + ((size_t)h * p.frames + frame_of(p, dir, step)) * (size_t)kMBytes; };
+    auto ctile = [&](int step) {
+        return reinterpret_cast<const uint8_t *>(p.ws_c + ((size_t)h * p.frames + frame_of(p, dir, step)) * kD * kD);
+    };
+    uint32_t m_loads = 0, c_loads = 0;  // copies issued, for the drain
+    if (steps >= 1) {
+        load64k(sm.m, mtile(1), sm.b(kBarM));
+        load64k(sm.c, ctile(1), sm.b(kBarC));
+        m_loads = c_loads = 1;
+    }
+    if (steps >= 2) {
+        load64k(sm.m + (uint32_t)kMBytes, mtile(2), sm.b(kBarM + 1));
+        m_loads = 2;
+    }
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, true);
+    const uint32_t t_d = tmem, t_hi = tmem + 128u, t_lo = tmem + 192u;
+    bool ok = wait_bar(sm, kBarA, 0u, p, kWhereA);  // S_0 split in tensor memory
+    if (ok) ptx::tc_fence_after();
+    for (int s = 1; ok && s <= steps; ++s) {
+        const int buf = (s - 1) & 1;
+        ok = wait_bar(sm, kBarM + buf, (uint32_t)(((s - 1) >> 1) & 1), p, kWhereM);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint64_t mh = ptx::sdesc_sw128(sm.m + (uint32_t)(buf * kMBytes), 16384, 1024);
+        const uint64_t ml = mh + (uint64_t)(32768 >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint64_t off = (uint64_t)((kk * 2048) >> 4);  // 16 rows of M' per MMA
+            ptx::mma_ts(t_d, t_hi + (uint32_t)(kk * 8), mh + off, idesc, kk > 0 ? 1u : 0u);
+            ptx::mma_ts(t_d, t_hi + (uint32_t)(kk * 8), ml + off, idesc, 1u);
+            ptx::mma_ts(t_d, t_lo + (uint32_t)(kk * 8), mh + off, idesc, 1u);
+        }
+        ptx::tc_commit(sm.b(kBarD));
+        // the MMAs have read this M' buffer: refill it two steps ahead
+        ok = wait_bar(sm, kBarD, (uint32_t)((s - 1) & 1), p, kWhereD);
+        if (!ok) break;
+        if (s + 2 <= steps) {
+            load64k(sm.m + (uint32_t)(buf * kMBytes), mtile(s + 2), sm.b(kBarM + buf));
+            ++m_loads;
+        }
+        // the rows have read C_s and written S_s's split
+        ok = wait_bar(sm, kBarA, (uint32_t)(s & 1), p, kWhereA);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if (s + 1 <= steps) {
+            load64k(sm.c, ctile(s + 1), sm.b(kBarC));
+            ++c_loads;
+        }
+    }
+    // every copy issued must have landed before the CTA exits
+    int never = 0;
+    for (uint32_t i = m_loads > 2u ? m_loads - 2u : 0u; i < m_loads; ++i)
+        ptx::mbar_wait(sm.b(kBarM + (int)(i & 1u)), (i >> 1) & 1u, &never, p.status, kDevTimeout | kWhereDrain);
+    if (c_loads > 0)
+        ptx::mbar_wait(sm.b(kBarC), (c_loads - 1u) & 1u, &never, p.status, kDevTimeout | kWhereDrain);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Row r: write the 32 values of columns 32 q .. 32 q + 31 of S as bf16 hi
+// and lo pairs into the A operands.
+__device__ __forceinline__ void split_store(const float (&v)[32], uint32_t t_hi, uint32_t t_lo, int q) {
+    uint32_t hi[16], lo[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+        const float2 hf = __bfloat1622float2(h2);
+        hi[e] = *reinterpret_cast<const uint32_t *>(&h2);
+        lo[e] = pack_bf16x2(v[2 * e] - hf.x, v[2 * e + 1] - hf.y);
+    }
+    ptx::tmem_st_32x32b_x16(t_hi + (uint32_t)(16 * q), hi);
+    ptx::tmem_st_32x32b_x16(t_lo + (uint32_t)(16 * q), lo);
+}
+
+__device__ void rows(const Params &p, const Smem &sm, uint32_t tmem, int h, int dir, int r) {
+    const int steps = p.frames - 2;
+    const uint32_t lane_base = (uint32_t)((r >> 5) * 32) << 16;
+    const uint32_t t_d = tmem + lane_base, t_hi = tmem + lane_base + 128u, t_lo = tmem + lane_base + 192u;
+    float *out = p.states + ((size_t)dir * p.heads + h) * (size_t)p.frames * kD * kD;
+    const int first = frame_of(p, dir, 0), last = frame_of(p, dir, p.frames - 1);
+    // S_0: half the text state (or zero)
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+        float v[32];
+        if (p.text_state != nullptr) {
+            const float *src = p.text_state + ((size_t)h * kD + r) * kD + 32 * q;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0.5f * src[e];
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+        }
+        float4 *d0 = reinterpret_cast<float4 *>(out + ((size_t)first * kD + r) * kD + 32 * q);
+        float4 *d1 = reinterpret_cast<float4 *>(out + ((size_t)last * kD + r) * kD + 32 * q);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float4 w = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            d0[e] = w;
+            if (steps <= 0 && p.frames >= 2) d1[e] = w;  // no written frame: the far anchor keeps S_0
+        }
+        split_store(v, t_hi, t_lo, q);
+    }
+    ptx::tmem_st_wait();
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(sm.b(kBarA));
+    bool ok = true;
+    for (int s = 1; ok && s <= steps; ++s) {
+        ok = __all_sync(0xffffffffu, wait_bar(sm, kBarD, (uint32_t)((s - 1) & 1), p, kWhereD));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        ok = __all_sync(0xffffffffu, wait_bar(sm, kBarC, (uint32_t)((s - 1) & 1), p, kWhereC));
+        if (!ok) break;
+        const int t = frame_of(p, dir, s);
+        float *dst = out + ((size_t)t * kD + r) * kD;
+        float *dlast = out + ((size_t)last * kD + r) * kD;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            uint32_t d[32];
+            ptx::tmem_ld_32x32b_x32(t_d + (uint32_t)(32 * q), d);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence(d);
+            float v[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(d[e]) + sm.cf[(32 * q + e) * kD + r];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float4 w = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                reinterpret_cast<float4 *>(dst + 32 * q)[e] = w;
+                if (s == steps) reinterpret_cast<float4 *>(dlast + 32 * q)[e] = w;  // the far anchor frame
+            }
+            if (s < steps) split_store(v, t_hi, t_lo, q);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(sm.b(kBarA));
+    }
+}
+
+}  // namespace sc
+
+__global__ void __launch_bounds__(sc::kThreads, 1) vda_scan_tc_kernel(const sc::Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    sc::Smem sm;
+    sm.m = base + sc::kSmemM;
+    sm.c = base + sc::kSmemC;
+    sm.bar = base + sc::kSmemBar;
+    sm.cf = reinterpret_cast<const float *>(smem + sc::kSmemC);
+    sm.abort_flag = reinterpret_cast<volatile int *>(smem + sc::kSmemMisc + 4);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + sc::kSmemMisc);
+    const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
+    const int h = (int)blockIdx.x, dir = (int)blockIdx.y;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(sm.b(sc::kBarM), 1);
+        ptx::mbar_init(sm.b(sc::kBarM + 1), 1);
+        ptx::mbar_init(sm.b(sc::kBarC), 1);
+        ptx::mbar_init(sm.b(sc::kBarD), 1);
+        ptx::mbar_init(sm.b(sc::kBarA), 128);
+        *sm.abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == sc::kCtlWarp) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), sc::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
+    if (warp == sc::kCtlWarp) {
+        if (lane == 0) sc::control(p, sm, tmem, h, dir);
+    } else {
+        sc::rows(p, sm, tmem, h, dir, (int)threadIdx.x);
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == sc::kCtlWarp) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, sc::kTmemCols);
+    }
+}
+
 // [n, ld] bf16 row-major, boxes of box_rows rows x 64 columns, 128-byte swizzle.
 bool make_map(CUtensorMap *m, const void *ptr, int64_t n, int ld, int box_rows) {
     EncodeTiledFn enc = tensor_map_encoder();
@@ -647,6 +905,32 @@ fv_status launch_vda_stats_tc(const DeltaLaunch &a, float *ws_m, float *ws_c, cu
     p.num_units = (frames - 2) * a.heads;
     const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
     vda_stats_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
+}
+
+fv_status launch_vda_scan_tc(const DeltaLaunch &a, const float *ws_m, const float *ws_c, cudaStream_t stream) {
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FV_ERR_LAUNCH;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(vda_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     sc::kSmemBytes) != cudaSuccess)
+                return FV_ERR_LAUNCH;
+            attr_set[dev] = true;
+        }
+    }
+    sc::Params p;
+    p.text_state = a.text_state;
+    p.ws_m = reinterpret_cast<const uint8_t *>(ws_m);
+    p.ws_c = ws_c;
+    p.states = a.states;
+    p.status = a.status;
+    p.frames = (int)(a.n / a.frame_tokens);
+    p.heads = a.heads;
+    vda_scan_tc_kernel<<<dim3(a.heads, 2), sc::kThreads, sc::kSmemBytes, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
 }
 
