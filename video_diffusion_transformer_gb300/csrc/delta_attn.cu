@@ -13,12 +13,12 @@
 //             frame after it.
 //
 // Four kernels:
-//   stats   (frame, head; tensor cores, delta_tc.cu): I + A_t -> ws_m, B_t -> ws_c
-//   solve   (frame, head; float32): Gauss-Jordan on [I + A_t | B_t^T] in registers,
-//                          M'_t = Diag(alpha_t) (I + A_t)^{-1} -> ws_m (bf16 hi/lo tiles),
-//                          C_t^T = (B_t (I + A_t)^{-1})^T -> ws_c
-//   scan    (head, direction; tensor cores, delta_tc.cu): S <- S M'_t + C_t,
-//           frame by frame, split-bf16 products with float32 accumulation
+//   stats   (frame, head; tensor cores, delta_tc.cu): I + A_t -> ws_m, B_t^T -> ws_c
+//   solve   (frame, head; float32): Gauss-Jordan inversion of I + A_t in registers,
+//           M_t = (I + A_t)^{-1} -> ws_m as bf16 hi/lo operand tiles
+//   scan    (head, direction; tensor cores, delta_tc.cu): S <- U M_t with
+//           U = S Diag(alpha_t) + B_t, frame by frame, split-bf16 products
+//           with float32 accumulation
 //   readout (chunk rows, head; tensor cores, delta_tc.cu): o = (S_fwd[p] + S_rev[n]) q_hat,
 //           rounded to bf16
 // The scan is the only sequential part: 2 H chains of F - 2 128x128x128 steps.
@@ -38,44 +38,35 @@ constexpr size_t kMat = (size_t)kDv * kDv;
 
 
 // ------------------------------------------------------------------ solve
-// Gauss-Jordan elimination on the 128 x 256 matrix [I + A | B^T] of frame t
-// of head h: after the 128 pivot steps the left half holds M = (I + A)^{-1}
-// and the right half X = M B^T, whose transpose is C = B M (M is symmetric).
-// No pivoting is needed: I + A is symmetric positive definite with every
-// Schur complement >= I (A is a sum of beta-weighted outer products,
-// beta >= 0), so every pivot is >= 1.  The matrix lives in registers: thread
-// (ty, tx) holds rows ty*8 .. ty*8+7 and columns tx*8 .. tx*8+7 of both
-// halves.  Each step broadcasts the pivot row and pivot column through shared
-// memory (two alternating buffers, one barrier per step).
-// Written out for the tensor-core scan: M' = Diag(alpha_t) M (the decay
-// folded into the scan's multiplier, S_{t-1} Diag(alpha_t) M = S_{t-1} M') as
-// two bf16 operand tiles, hi and lo (M' = hi + lo to 2^-17), each
-// [2 column halves][128 rows][64 columns] in the 128-byte swizzled layout
-// (16-byte chunk j of row q at chunk j ^ (q % 8)), in the frame's 64 KB of
-// ws_m; and C^T = X, float32 row-major, in ws_c.
-__global__ void __launch_bounds__(kDThreads, 1)
-    vda_solve_kernel(const float *__restrict__ alpha, int frames, float *__restrict__ ws_m,
-                     float *__restrict__ ws_c) {
-    __shared__ __align__(16) float rowbuf[2][2 * kDv];
+// Gauss-Jordan inversion of G = I + A_t of frame t of head h in place:
+// after the 128 pivot steps G holds M = (I + A_t)^{-1}.  No pivoting is
+// needed: I + A is symmetric positive definite with every Schur complement
+// >= I (A is a sum of beta-weighted outer products, beta >= 0), so every
+// pivot is >= 1.  The matrix lives in registers: thread (ty, tx) holds rows
+// ty*8 .. ty*8+7 and columns tx*8 .. tx*8+7.  Each step broadcasts the pivot
+// row and pivot column through shared memory (two alternating buffers, one
+// barrier per step) and applies one update to every element: row i loses f_i
+// times the pivot row divided by the pivot, with f_k - 1 for the pivot row
+// itself (so it becomes the divided row), and the pivot column first set to
+// the identity's column (so it becomes column k of the inverse).
+// Written out for the tensor-core scan as two bf16 operand tiles, hi and lo
+// (M = hi + lo to 2^-17), each [2 column halves][128 rows][64 columns] in the
+// 128-byte swizzled layout (16-byte chunk j of row q at chunk j ^ (q % 8)),
+// in the frame's 64 KB of ws_m.
+__global__ void __launch_bounds__(kDThreads, 1) vda_solve_kernel(int frames, float *__restrict__ ws_m) {
+    __shared__ __align__(16) float rowbuf[2][kDv];
     __shared__ __align__(16) float colbuf[2][kDv];
     const int t = (int)blockIdx.x + 1;
     const int h = (int)blockIdx.y;
     const size_t base = ((size_t)h * frames + t) * kMat;
     const int tid = (int)threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    float g[8][8], x[8][8];
+    float g[8][8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const float4 *src = reinterpret_cast<const float4 *>(ws_m + base + (size_t)(ty * 8 + i) * kDv + tx * 8);
         const float4 a0 = src[0], a1 = src[1];
         g[i][0] = a0.x, g[i][1] = a0.y, g[i][2] = a0.z, g[i][3] = a0.w;
         g[i][4] = a1.x, g[i][5] = a1.y, g[i][6] = a1.z, g[i][7] = a1.w;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {  // X = B^T: x[i][j] = B[tx*8 + j][ty*8 + i]
-        const float4 *src = reinterpret_cast<const float4 *>(ws_c + base + (size_t)(tx * 8 + j) * kDv + ty * 8);
-        const float4 b0 = src[0], b1 = src[1];
-        x[0][j] = b0.x, x[1][j] = b0.y, x[2][j] = b0.z, x[3][j] = b0.w;
-        x[4][j] = b1.x, x[5][j] = b1.y, x[6][j] = b1.z, x[7][j] = b1.w;
     }
     for (int kb = 0; kb < kDv / 8; ++kb) {
         const bool own_row = ty == kb, own_col = tx == kb;
@@ -86,11 +77,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
             float *cb = colbuf[kk & 1];
             if (own_row) {
                 float4 *dg = reinterpret_cast<float4 *>(rb + tx * 8);
-                float4 *dx = reinterpret_cast<float4 *>(rb + kDv + tx * 8);
                 dg[0] = make_float4(g[kk][0], g[kk][1], g[kk][2], g[kk][3]);
                 dg[1] = make_float4(g[kk][4], g[kk][5], g[kk][6], g[kk][7]);
-                dx[0] = make_float4(x[kk][0], x[kk][1], x[kk][2], x[kk][3]);
-                dx[1] = make_float4(x[kk][4], x[kk][5], x[kk][6], x[kk][7]);
             }
             if (own_col) {
                 float4 *dc = reinterpret_cast<float4 *>(cb + ty * 8);
@@ -99,29 +87,18 @@ __global__ void __launch_bounds__(kDThreads, 1)
             }
             __syncthreads();
             const float p = 1.0f / rb[k];
-            float rg[8], rx[8], f[8];
+            float rg[8], f[8];
             {
                 const float4 *sg = reinterpret_cast<const float4 *>(rb + tx * 8);
-                const float4 *sx = reinterpret_cast<const float4 *>(rb + kDv + tx * 8);
                 const float4 *sc = reinterpret_cast<const float4 *>(cb + ty * 8);
-                const float4 g0 = sg[0], g1 = sg[1], x0 = sx[0], x1 = sx[1], c0 = sc[0], c1 = sc[1];
+                const float4 g0 = sg[0], g1 = sg[1], c0 = sc[0], c1 = sc[1];
                 rg[0] = g0.x, rg[1] = g0.y, rg[2] = g0.z, rg[3] = g0.w;
                 rg[4] = g1.x, rg[5] = g1.y, rg[6] = g1.z, rg[7] = g1.w;
-                rx[0] = x0.x, rx[1] = x0.y, rx[2] = x0.z, rx[3] = x0.w;
-                rx[4] = x1.x, rx[5] = x1.y, rx[6] = x1.z, rx[7] = x1.w;
                 f[0] = c0.x, f[1] = c0.y, f[2] = c0.z, f[3] = c0.w;
                 f[4] = c1.x, f[5] = c1.y, f[6] = c1.z, f[7] = c1.w;
             }
-            // One update for every element: row i loses f_i times the pivot row
-            // divided by the pivot, with f_k - 1 for the pivot row itself (so it
-            // becomes the divided row), and the pivot column first set to the
-            // identity's column (so it becomes column k of the inverse:
-            // -f_i / pivot, and 1 / pivot on the diagonal).
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                rg[j] *= p;
-                rx[j] *= p;
-            }
+            for (int j = 0; j < 8; ++j) rg[j] *= p;
             if (own_col) {
                 rg[kk] = p;
 #pragma unroll
@@ -129,25 +106,19 @@ __global__ void __launch_bounds__(kDThreads, 1)
             }
             if (own_row) f[kk] -= 1.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    g[i][j] = fmaf(-f[i], rg[j], g[i][j]);
-                    x[i][j] = fmaf(-f[i], rx[j], x[i][j]);
-                }
-            }
+                for (int j = 0; j < 8; ++j) g[i][j] = fmaf(-f[i], rg[j], g[i][j]);
         }
     }
-    const float *al = alpha + ((size_t)h * frames + t) * kDv;
     uint8_t *mo = reinterpret_cast<uint8_t *>(ws_m + base);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int q = ty * 8 + i;
-        const float a = al[q];
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float v0 = a * g[i][2 * e], v1 = a * g[i][2 * e + 1];
+            const float v0 = g[i][2 * e], v1 = g[i][2 * e + 1];
             const __nv_bfloat162 h2 = __floats2bfloat162_rn(v0, v1);
             const float2 hf = __bfloat1622float2(h2);
             const __nv_bfloat162 l2 = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
@@ -157,12 +128,6 @@ __global__ void __launch_bounds__(kDThreads, 1)
         const size_t off = (size_t)(tx >> 3) * 16384 + (size_t)q * 128 + (size_t)(((tx & 7) ^ (q & 7)) << 4);
         *reinterpret_cast<uint4 *>(mo + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4 *>(mo + 32768 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {  // C^T = X, row-major
-        float4 *dst = reinterpret_cast<float4 *>(ws_c + base + (size_t)(ty * 8 + i) * kDv + tx * 8);
-        dst[0] = make_float4(x[i][0], x[i][1], x[i][2], x[i][3]);
-        dst[1] = make_float4(x[i][4], x[i][5], x[i][6], x[i][7]);
     }
 }
 
@@ -175,7 +140,7 @@ fv_status launch_delta_attn(const DeltaLaunch &a, cudaStream_t stream) {
     if (frames > 2) {
         const fv_status st = launch_vda_stats_tc(a, ws_m, ws_c, stream);
         if (st != FV_OK) return st;
-        vda_solve_kernel<<<dim3(frames - 2, a.heads), kDThreads, 0, stream>>>(a.alpha, frames, ws_m, ws_c);
+        vda_solve_kernel<<<dim3(frames - 2, a.heads), kDThreads, 0, stream>>>(frames, ws_m);
     }
     const fv_status st = launch_vda_scan_tc(a, ws_m, ws_c, stream);
     if (st != FV_OK) return st;

@@ -20,7 +20,7 @@
 //     MN-major (channels contiguous); D_A and D_B in tensor memory, double
 //     buffered across units;
 //   warps 0-3 (the epilogue): thread = row i of D; writes row i of I + A_t and
-//     of B_t (float32) to the workspace.
+//     column i of B_t^T (float32) to the workspace.
 // All waits are bounded; a wait that runs out records kDevTimeout | where.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -263,10 +263,18 @@ __device__ void epilogue(const Params &p, const Smem &sm, uint32_t tmem, int t) 
                     for (int e = 0; e < 32; ++e)
                         if (e == (t & 31)) r[e] = __float_as_uint(__uint_as_float(r[e]) + 1.0f);
                 }
+                if (m == 0) {
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    *reinterpret_cast<uint4 *>(dst + 32 * c4 + 4 * v) =
-                        make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+                    for (int v = 0; v < 8; ++v)
+                        *reinterpret_cast<uint4 *>(dst + 32 * c4 + 4 * v) =
+                            make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+                } else {
+                    // B_t transposed: column c of B is row c of ws_c (the
+                    // warp's 32 rows t form one 128-byte segment)
+                    float *bt = p.ws_c + ((size_t)head * p.frames + frame) * kD * kD + t;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) bt[(size_t)(32 * c4 + e) * kD] = __uint_as_float(r[e]);
+                }
             }
         }
         ptx::tc_fence_before();
@@ -601,47 +609,50 @@ __global__ void __launch_bounds__(ro::kThreads, 1)
 }
 
 // =================================================================== scan
-// One (head, direction) chain: S <- S M'_t + C_t frame by frame, every state
-// stored, on the tensor cores.  S_{t-1} lives in tensor memory as two bf16
-// operands (S = S_hi + S_lo to 2^-17); M'_t arrives from the solve as two bf16
-// operand tiles (hi, lo) already in the 128-byte swizzled MN-major layout;
-// D = S_hi M'_hi + S_hi M'_lo + S_lo M'_hi (24 MMAs, float32 accumulate; the
-// dropped S_lo M'_lo is below 2^-17 of the product).  C_t arrives transposed
-// (C^T, float32) so that thread r reads row r of C conflict-free.
-// 160 threads: warps 0-3 own the 128 state rows (TMEM lanes): they add C_t to
-// D, store S_t, and write its bf16 split for the next step; warp 4 (one
-// thread) loads M' (two buffers) and C (one buffer) by bulk copy and issues
-// the MMAs.
+// One (head, direction) chain, every state stored, on the tensor cores:
+//   S_t = U_t M_t,  U_t = S_{t-1} Diag(alpha_t) + B_t,  M_t = (I + A_t)^{-1}
+// (the same state as S_{t-1} Diag(alpha_t) M_t + B_t M_t).  U_t lives in
+// tensor memory as two bf16 operands (U = U_hi + U_lo to 2^-17); M_t arrives
+// from the solve as two bf16 operand tiles (hi, lo) already in the 128-byte
+// swizzled MN-major layout; D = U_hi M_hi + U_hi M_lo + U_lo M_hi (24 MMAs,
+// float32 accumulate; the dropped U_lo M_lo is below 2^-17 of the product).
+// B_t arrives transposed (float32) so that thread r reads row r of B_t
+// without bank conflicts.
+// 160 threads: warps 0-3 own the 128 state rows (TMEM lanes): they store
+// S_t = D, form U_{t+1} from it, alpha_{t+1} and B_{t+1}, and write its bf16
+// split; warp 4 (one thread) loads M (two buffers) and B (one buffer) by bulk
+// copy and issues the MMAs.
 namespace sc {
 
 constexpr int kThreads = 160;
 constexpr int kCtlWarp = 4;
-constexpr uint32_t kTmemCols = 256;            // D (0-127), S_hi (128-191), S_lo (192-255)
-constexpr int kMBytes = 2 * 32768;             // M'_t: hi and lo operand tiles
-constexpr int kCBytes = kD * kD * 4;           // C_t^T, float32
+constexpr uint32_t kTmemCols = 256;            // D (0-127), U_hi (128-191), U_lo (192-255)
+constexpr int kMBytes = 2 * 32768;             // M_t: hi and lo operand tiles
+constexpr int kBBytes = kD * kD * 4;           // B_t^T, float32
 constexpr int kSmemM = 0;                      // two buffers
-constexpr int kSmemC = kSmemM + 2 * kMBytes;
+constexpr int kSmemB = kSmemM + 2 * kMBytes;
 constexpr int kBarM = 0;                       // two
-constexpr int kBarC = 2, kBarD = 3, kBarA = 4;
+constexpr int kBarB = 2, kBarD = 3, kBarA = 4;
 constexpr int kNumBars = 5;
-constexpr int kSmemBar = kSmemC + kCBytes;
+constexpr int kSmemBar = kSmemB + kBBytes;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
 constexpr int kSmemBytes = kSmemMisc + 16 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-constexpr int kWhereM = 1, kWhereC = 2, kWhereD = 3, kWhereA = 4, kWhereDrain = 5;
+constexpr int kWhereM = 1, kWhereB = 2, kWhereD = 3, kWhereA = 4, kWhereDrain = 5;
 
 struct Params {
     const float *text_state;  // [heads, 128, 128] or null
-    const uint8_t *ws_m;      // per (head, frame): M'_t hi and lo tiles (64 KB)
-    const float *ws_c;        // per (head, frame): C_t^T
+    const float *alpha;       // [heads, frames, 128]
+    const uint8_t *ws_m;      // per (head, frame): M_t hi and lo tiles (64 KB)
+    const float *ws_c;        // per (head, frame): B_t^T
     float *states;            // [2, heads, frames, 128, 128]
     int *status;
     int frames, heads;
 };
 
 struct Smem {
-    uint32_t m, c, bar;
-    const float *cf;  // the C buffer, generic address
+    uint32_t m, bq, bar;
+    const float *bf;  // the B buffer, generic address
     volatile int *abort_flag;
     __device__ uint32_t b(int i) const { return bar + 8u * (uint32_t)i; }
 };
@@ -670,14 +681,16 @@ __device__ __forceinline__ int frame_of(const Params &p, int dir, int step) {
 __device__ void control(const Params &p, const Smem &sm, uint32_t tmem, int h, int dir) {
     const int steps = p.frames - 2;
     auto mtile = [&](int step) { return p.ws_m + ((size_t)h * p.frames + frame_of(p, dir, step)) * (size_t)kMBytes; };
-    auto ctile = [&](int step) {
+    auto btile = [&](int step) {
         return reinterpret_cast<const uint8_t *>(p.ws_c + ((size_t)h * p.frames + frame_of(p, dir, step)) * kD * kD);
     };
-    uint32_t m_loads = 0, c_loads = 0;  // copies issued, for the drain
+    // B_k completes phase k - 1 of kBarB; the rows read it while forming U_k
+    // (for k = 1 before the first step, else in the epilogue of step k - 1)
+    uint32_t m_loads = 0, b_loads = 0;  // copies issued, for the drain
     if (steps >= 1) {
         load64k(sm.m, mtile(1), sm.b(kBarM));
-        load64k(sm.c, ctile(1), sm.b(kBarC));
-        m_loads = c_loads = 1;
+        load64k(sm.bq, btile(1), sm.b(kBarB));
+        m_loads = b_loads = 1;
     }
     if (steps >= 2) {
         load64k(sm.m + (uint32_t)kMBytes, mtile(2), sm.b(kBarM + 1));
@@ -685,8 +698,14 @@ __device__ void control(const Params &p, const Smem &sm, uint32_t tmem, int h, i
     }
     constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, true);
     const uint32_t t_d = tmem, t_hi = tmem + 128u, t_lo = tmem + 192u;
-    bool ok = wait_bar(sm, kBarA, 0u, p, kWhereA);  // S_0 split in tensor memory
-    if (ok) ptx::tc_fence_after();
+    bool ok = wait_bar(sm, kBarA, 0u, p, kWhereA);  // U_1 split in tensor memory, B_1 read
+    if (ok) {
+        ptx::tc_fence_after();
+        if (steps >= 2) {
+            load64k(sm.bq, btile(2), sm.b(kBarB));
+            ++b_loads;
+        }
+    }
     for (int s = 1; ok && s <= steps; ++s) {
         const int buf = (s - 1) & 1;
         ok = wait_bar(sm, kBarM + buf, (uint32_t)(((s - 1) >> 1) & 1), p, kWhereM);
@@ -696,34 +715,34 @@ __device__ void control(const Params &p, const Smem &sm, uint32_t tmem, int h, i
         const uint64_t ml = mh + (uint64_t)(32768 >> 4);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint64_t off = (uint64_t)((kk * 2048) >> 4);  // 16 rows of M' per MMA
+            const uint64_t off = (uint64_t)((kk * 2048) >> 4);  // 16 rows of M per MMA
             ptx::mma_ts(t_d, t_hi + (uint32_t)(kk * 8), mh + off, idesc, kk > 0 ? 1u : 0u);
             ptx::mma_ts(t_d, t_hi + (uint32_t)(kk * 8), ml + off, idesc, 1u);
             ptx::mma_ts(t_d, t_lo + (uint32_t)(kk * 8), mh + off, idesc, 1u);
         }
         ptx::tc_commit(sm.b(kBarD));
-        // the MMAs have read this M' buffer: refill it two steps ahead
+        // the MMAs have read this M buffer: refill it two steps ahead
         ok = wait_bar(sm, kBarD, (uint32_t)((s - 1) & 1), p, kWhereD);
         if (!ok) break;
         if (s + 2 <= steps) {
             load64k(sm.m + (uint32_t)(buf * kMBytes), mtile(s + 2), sm.b(kBarM + buf));
             ++m_loads;
         }
-        // the rows have read C_s and written S_s's split
+        // the rows have stored S_s, read B_{s+1} and written U_{s+1}'s split
         ok = wait_bar(sm, kBarA, (uint32_t)(s & 1), p, kWhereA);
         if (!ok) break;
         ptx::tc_fence_after();
-        if (s + 1 <= steps) {
-            load64k(sm.c, ctile(s + 1), sm.b(kBarC));
-            ++c_loads;
+        if (s + 2 <= steps) {
+            load64k(sm.bq, btile(s + 2), sm.b(kBarB));
+            ++b_loads;
         }
     }
     // every copy issued must have landed before the CTA exits
     int never = 0;
     for (uint32_t i = m_loads > 2u ? m_loads - 2u : 0u; i < m_loads; ++i)
         ptx::mbar_wait(sm.b(kBarM + (int)(i & 1u)), (i >> 1) & 1u, &never, p.status, kDevTimeout | kWhereDrain);
-    if (c_loads > 0)
-        ptx::mbar_wait(sm.b(kBarC), (c_loads - 1u) & 1u, &never, p.status, kDevTimeout | kWhereDrain);
+    if (b_loads > 0)
+        ptx::mbar_wait(sm.b(kBarB), (b_loads - 1u) & 1u, &never, p.status, kDevTimeout | kWhereDrain);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -746,45 +765,63 @@ __device__ __forceinline__ void split_store(const float (&v)[32], uint32_t t_hi,
     ptx::tmem_st_32x32b_x16(t_lo + (uint32_t)(16 * q), lo);
 }
 
+// U = S Diag(alpha) + B for columns 32 q .. 32 q + 31 of row r (B from the
+// transposed buffer), written as the bf16 split
+__device__ __forceinline__ void form_u(const float (&v)[32], const float *al, const float *bt, int r, int q,
+                                       uint32_t t_hi, uint32_t t_lo) {
+    float u[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) u[e] = fmaf(v[e], al[32 * q + e], bt[(32 * q + e) * kD + r]);
+    split_store(u, t_hi, t_lo, q);
+}
+
 __device__ void rows(const Params &p, const Smem &sm, uint32_t tmem, int h, int dir, int r) {
     const int steps = p.frames - 2;
     const uint32_t lane_base = (uint32_t)((r >> 5) * 32) << 16;
     const uint32_t t_d = tmem + lane_base, t_hi = tmem + lane_base + 128u, t_lo = tmem + lane_base + 192u;
     float *out = p.states + ((size_t)dir * p.heads + h) * (size_t)p.frames * kD * kD;
     const int first = frame_of(p, dir, 0), last = frame_of(p, dir, p.frames - 1);
-    // S_0: half the text state (or zero)
+    auto alpha_of = [&](int step) { return p.alpha + ((size_t)h * p.frames + frame_of(p, dir, step)) * kD; };
+    // S_0: half the text state (or zero); U_1 from it
+    bool ok = true;
+    if (steps >= 1) ok = __all_sync(0xffffffffu, wait_bar(sm, kBarB, 0u, p, kWhereB));
+    if (ok) {
+        const float *al = steps >= 1 ? alpha_of(1) : nullptr;
 #pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-        float v[32];
-        if (p.text_state != nullptr) {
-            const float *src = p.text_state + ((size_t)h * kD + r) * kD + 32 * q;
+        for (int q = 0; q < 4; ++q) {
+            float v[32];
+            if (p.text_state != nullptr) {
+                const float *src = p.text_state + ((size_t)h * kD + r) * kD + 32 * q;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = 0.5f * src[e];
-        } else {
+                for (int e = 0; e < 32; ++e) v[e] = 0.5f * src[e];
+            } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+                for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+            }
+            float4 *d0 = reinterpret_cast<float4 *>(out + ((size_t)first * kD + r) * kD + 32 * q);
+            float4 *d1 = reinterpret_cast<float4 *>(out + ((size_t)last * kD + r) * kD + 32 * q);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float4 w = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                d0[e] = w;
+                if (steps <= 0 && p.frames >= 2) d1[e] = w;  // no written frame: the far anchor keeps S_0
+            }
+            if (steps >= 1) form_u(v, al, sm.bf, r, q, t_hi, t_lo);
         }
-        float4 *d0 = reinterpret_cast<float4 *>(out + ((size_t)first * kD + r) * kD + 32 * q);
-        float4 *d1 = reinterpret_cast<float4 *>(out + ((size_t)last * kD + r) * kD + 32 * q);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float4 w = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-            d0[e] = w;
-            if (steps <= 0 && p.frames >= 2) d1[e] = w;  // no written frame: the far anchor keeps S_0
-        }
-        split_store(v, t_hi, t_lo, q);
+        ptx::tmem_st_wait();
     }
-    ptx::tmem_st_wait();
     ptx::tc_fence_before();
     ptx::mbar_arrive(sm.b(kBarA));
-    bool ok = true;
     for (int s = 1; ok && s <= steps; ++s) {
         ok = __all_sync(0xffffffffu, wait_bar(sm, kBarD, (uint32_t)((s - 1) & 1), p, kWhereD));
         if (!ok) break;
         ptx::tc_fence_after();
-        ok = __all_sync(0xffffffffu, wait_bar(sm, kBarC, (uint32_t)((s - 1) & 1), p, kWhereC));
-        if (!ok) break;
+        if (s < steps) {
+            ok = __all_sync(0xffffffffu, wait_bar(sm, kBarB, (uint32_t)(s & 1), p, kWhereB));
+            if (!ok) break;
+        }
         const int t = frame_of(p, dir, s);
+        const float *al = s < steps ? alpha_of(s + 1) : nullptr;
         float *dst = out + ((size_t)t * kD + r) * kD;
         float *dlast = out + ((size_t)last * kD + r) * kD;
 #pragma unroll 1
@@ -795,14 +832,14 @@ __device__ void rows(const Params &p, const Smem &sm, uint32_t tmem, int h, int 
             ptx::reg_fence(d);
             float v[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(d[e]) + sm.cf[(32 * q + e) * kD + r];
+            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(d[e]);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float4 w = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                 reinterpret_cast<float4 *>(dst + 32 * q)[e] = w;
                 if (s == steps) reinterpret_cast<float4 *>(dlast + 32 * q)[e] = w;  // the far anchor frame
             }
-            if (s < steps) split_store(v, t_hi, t_lo, q);
+            if (s < steps) form_u(v, al, sm.bf, r, q, t_hi, t_lo);
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
@@ -819,9 +856,9 @@ __global__ void __launch_bounds__(sc::kThreads, 1) vda_scan_tc_kernel(const sc::
     uint8_t *smem = smem_raw + (base - raw);
     sc::Smem sm;
     sm.m = base + sc::kSmemM;
-    sm.c = base + sc::kSmemC;
+    sm.bq = base + sc::kSmemB;
     sm.bar = base + sc::kSmemBar;
-    sm.cf = reinterpret_cast<const float *>(smem + sc::kSmemC);
+    sm.bf = reinterpret_cast<const float *>(smem + sc::kSmemB);
     sm.abort_flag = reinterpret_cast<volatile int *>(smem + sc::kSmemMisc + 4);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + sc::kSmemMisc);
     const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
@@ -829,7 +866,7 @@ __global__ void __launch_bounds__(sc::kThreads, 1) vda_scan_tc_kernel(const sc::
     if (threadIdx.x == 0) {
         ptx::mbar_init(sm.b(sc::kBarM), 1);
         ptx::mbar_init(sm.b(sc::kBarM + 1), 1);
-        ptx::mbar_init(sm.b(sc::kBarC), 1);
+        ptx::mbar_init(sm.b(sc::kBarB), 1);
         ptx::mbar_init(sm.b(sc::kBarD), 1);
         ptx::mbar_init(sm.b(sc::kBarA), 128);
         *sm.abort_flag = 0;
@@ -924,6 +961,7 @@ fv_status launch_vda_scan_tc(const DeltaLaunch &a, const float *ws_m, const floa
     }
     sc::Params p;
     p.text_state = a.text_state;
+    p.alpha = a.alpha;
     p.ws_m = reinterpret_cast<const uint8_t *>(ws_m);
     p.ws_c = ws_c;
     p.states = a.states;

@@ -72,12 +72,12 @@ struct DeltaLaunch {
     int num_sms;
 };
 
-// The per-frame sums I + A_t -> ws_m and B_t -> ws_c of frames 1 .. F-2 on the
-// tensor cores (layout [heads, frames, 128, 128]).
+// The per-frame sums I + A_t -> ws_m and B_t^T -> ws_c of frames 1 .. F-2 on
+// the tensor cores (layout [heads, frames, 128, 128]).
 fv_status launch_vda_stats_tc(const DeltaLaunch &a, float *ws_m, float *ws_c, cudaStream_t stream);
-// The forward and reverse state scans S <- S M'_t + C_t on the tensor cores
-// (split-bf16 products); ws_m holds M'_t as hi/lo bf16 operand tiles, ws_c
-// holds C_t^T, both as the solve writes them.
+// The forward and reverse state scans S <- (S Diag(alpha_t) + B_t) M_t on the
+// tensor cores (split-bf16 products); ws_m holds M_t = (I + A_t)^{-1} as hi/lo
+// bf16 operand tiles (as the solve writes them), ws_c holds B_t^T.
 fv_status launch_vda_scan_tc(const DeltaLaunch &a, const float *ws_m, const float *ws_c, cudaStream_t stream);
 // o = (S_fwd[p] + S_rev[n]) q / |q| for every token, on the tensor cores;
 // wsplit: scratch of heads * chunks * 2 * 128 * 128 bf16.
