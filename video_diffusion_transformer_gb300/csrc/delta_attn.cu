@@ -53,7 +53,7 @@ constexpr size_t kMat = (size_t)kDv * kDv;
 // (M = hi + lo to 2^-17), each [2 column halves][128 rows][64 columns] in the
 // 128-byte swizzled layout (16-byte chunk j of row q at chunk j ^ (q % 8)),
 // in the frame's 64 KB of ws_m.
-__global__ void __launch_bounds__(kDThreads, 1) vda_solve_kernel(int frames, float *__restrict__ ws_m) {
+__global__ void __launch_bounds__(kDThreads, 2) vda_solve_kernel(int frames, float *__restrict__ ws_m) {
     __shared__ __align__(16) float rowbuf[2][kDv];
     __shared__ __align__(16) float colbuf[2][kDv];
     const int t = (int)blockIdx.x + 1;

@@ -628,13 +628,15 @@ constexpr int kThreads = 160;
 constexpr int kCtlWarp = 4;
 constexpr uint32_t kTmemCols = 256;            // D (0-127), U_hi (128-191), U_lo (192-255)
 constexpr int kMBytes = 2 * 32768;             // M_t: hi and lo operand tiles
-constexpr int kBBytes = kD * kD * 4;           // B_t^T, float32
+constexpr int kABytes = kD * 4;                // alpha_t, float32
 constexpr int kSmemM = 0;                      // two buffers
-constexpr int kSmemB = kSmemM + 2 * kMBytes;
+constexpr int kSmemAl = kSmemM + 2 * kMBytes;  // alpha of the frame of the next U
 constexpr int kBarM = 0;                       // two
 constexpr int kBarB = 2, kBarD = 3, kBarA = 4;
 constexpr int kNumBars = 5;
-constexpr int kSmemBar = kSmemB + kBBytes;
+constexpr int kStageLd = kD + 4;               // staged state rows, padded (conflict-free 16-byte stores)
+constexpr int kSmemStage = kSmemAl + kABytes;  // [128 rows][kStageLd] float
+constexpr int kSmemBar = kSmemStage + kD * kStageLd * 4;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
 constexpr int kSmemBytes = kSmemMisc + 16 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -651,8 +653,9 @@ struct Params {
 };
 
 struct Smem {
-    uint32_t m, bq, bar;
-    const float *bf;  // the B buffer, generic address
+    uint32_t m, al, bar;
+    const float *af;  // the alpha buffer, generic address
+    float *stage;     // state rows on their way to global memory
     volatile int *abort_flag;
     __device__ uint32_t b(int i) const { return bar + 8u * (uint32_t)i; }
 };
@@ -674,6 +677,12 @@ __device__ __forceinline__ void load64k(uint32_t dst, const uint8_t *src, uint32
     for (int i = 0; i < 4; ++i) bulk_copy(dst + 16384u * (uint32_t)i, src + 16384 * i, bar);
 }
 
+__device__ __forceinline__ void bulk_copy_n(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ int frame_of(const Params &p, int dir, int step) {
     return dir == 0 ? step : p.frames - 1 - step;
 }
@@ -681,15 +690,19 @@ __device__ __forceinline__ int frame_of(const Params &p, int dir, int step) {
 __device__ void control(const Params &p, const Smem &sm, uint32_t tmem, int h, int dir) {
     const int steps = p.frames - 2;
     auto mtile = [&](int step) { return p.ws_m + ((size_t)h * p.frames + frame_of(p, dir, step)) * (size_t)kMBytes; };
-    auto btile = [&](int step) {
-        return reinterpret_cast<const uint8_t *>(p.ws_c + ((size_t)h * p.frames + frame_of(p, dir, step)) * kD * kD);
+    // alpha_k of step k's frame (B_k the row threads fetch themselves)
+    auto load_b = [&](int step) {
+        const size_t f = (size_t)h * p.frames + frame_of(p, dir, step);
+        const uint32_t bar = sm.b(kBarB);
+        ptx::mbar_arrive_expect_tx(bar, (uint32_t)kABytes);
+        bulk_copy_n(sm.al, p.alpha + f * kD, (uint32_t)kABytes, bar);
     };
     // B_k completes phase k - 1 of kBarB; the rows read it while forming U_k
     // (for k = 1 before the first step, else in the epilogue of step k - 1)
     uint32_t m_loads = 0, b_loads = 0;  // copies issued, for the drain
     if (steps >= 1) {
         load64k(sm.m, mtile(1), sm.b(kBarM));
-        load64k(sm.bq, btile(1), sm.b(kBarB));
+        load_b(1);
         m_loads = b_loads = 1;
     }
     if (steps >= 2) {
@@ -702,7 +715,7 @@ __device__ void control(const Params &p, const Smem &sm, uint32_t tmem, int h, i
     if (ok) {
         ptx::tc_fence_after();
         if (steps >= 2) {
-            load64k(sm.bq, btile(2), sm.b(kBarB));
+            load_b(2);
             ++b_loads;
         }
     }
@@ -733,7 +746,7 @@ __device__ void control(const Params &p, const Smem &sm, uint32_t tmem, int h, i
         if (!ok) break;
         ptx::tc_fence_after();
         if (s + 2 <= steps) {
-            load64k(sm.bq, btile(s + 2), sm.b(kBarB));
+            load_b(s + 2);
             ++b_loads;
         }
     }
@@ -765,14 +778,35 @@ __device__ __forceinline__ void split_store(const float (&v)[32], uint32_t t_hi,
     ptx::tmem_st_32x32b_x16(t_lo + (uint32_t)(16 * q), lo);
 }
 
-// U = S Diag(alpha) + B for columns 32 q .. 32 q + 31 of row r (B from the
-// transposed buffer), written as the bf16 split
-__device__ __forceinline__ void form_u(const float (&v)[32], const float *al, const float *bt, int r, int q,
+// U = S Diag(alpha) + B for columns 32 q .. 32 q + 31 of the row (b: the
+// row of B), written as the bf16 split
+__device__ __forceinline__ void form_u(const float (&v)[32], const float *al, const float (&b)[kD], int q,
                                        uint32_t t_hi, uint32_t t_lo) {
     float u[32];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) u[e] = fmaf(v[e], al[32 * q + e], bt[(32 * q + e) * kD + r]);
+    for (int e = 0; e < 32; ++e) u[e] = fmaf(v[e], al[32 * q + e], b[32 * q + e]);
     split_store(u, t_hi, t_lo, q);
+}
+
+// Stage columns 32 q .. 32 q + 31 of row r
+__device__ __forceinline__ void stage_row(const Smem &sm, int r, int q, const float (&v)[32]) {
+    float4 *d = reinterpret_cast<float4 *>(sm.stage + (size_t)r * kStageLd + 32 * q);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) d[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+}
+
+// The warp's 32 staged rows to frame rows of dst (and of dst2 when given):
+// one whole 512-byte row per store instruction
+__device__ __forceinline__ void write_rows(const Smem &sm, int r, float *dst, float *dst2) {
+    __syncwarp();
+    const int lane = r & 31, r0 = r & ~31;
+#pragma unroll 4
+    for (int i = 0; i < 32; ++i) {
+        const float4 w = reinterpret_cast<const float4 *>(sm.stage + (size_t)(r0 + i) * kStageLd)[lane];
+        reinterpret_cast<float4 *>(dst + (size_t)(r0 + i) * kD)[lane] = w;
+        if (dst2 != nullptr) reinterpret_cast<float4 *>(dst2 + (size_t)(r0 + i) * kD)[lane] = w;
+    }
+    __syncwarp();
 }
 
 __device__ void rows(const Params &p, const Smem &sm, uint32_t tmem, int h, int dir, int r) {
@@ -781,13 +815,21 @@ __device__ void rows(const Params &p, const Smem &sm, uint32_t tmem, int h, int 
     const uint32_t t_d = tmem + lane_base, t_hi = tmem + lane_base + 128u, t_lo = tmem + lane_base + 192u;
     float *out = p.states + ((size_t)dir * p.heads + h) * (size_t)p.frames * kD * kD;
     const int first = frame_of(p, dir, 0), last = frame_of(p, dir, p.frames - 1);
-    auto alpha_of = [&](int step) { return p.alpha + ((size_t)h * p.frames + frame_of(p, dir, step)) * kD; };
+    // row r of B_k (B_k^T is stored, so a warp's loads are 128-byte
+    // segments), fetched into registers a step ahead of its use
+    float bn[kD];
+    auto fetch_b = [&](int step) {
+        const float *src = p.ws_c + ((size_t)h * p.frames + frame_of(p, dir, step)) * kD * kD + r;
+#pragma unroll
+        for (int c = 0; c < kD; ++c) bn[c] = src[(size_t)c * kD];
+    };
+    if (steps >= 1) fetch_b(1);
     // S_0: half the text state (or zero); U_1 from it
     bool ok = true;
     if (steps >= 1) ok = __all_sync(0xffffffffu, wait_bar(sm, kBarB, 0u, p, kWhereB));
     if (ok) {
-        const float *al = steps >= 1 ? alpha_of(1) : nullptr;
-#pragma unroll 1
+        const float *al = sm.af;
+#pragma unroll
         for (int q = 0; q < 4; ++q) {
             float v[32];
             if (p.text_state != nullptr) {
@@ -798,21 +840,18 @@ __device__ void rows(const Params &p, const Smem &sm, uint32_t tmem, int h, int 
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = 0.0f;
             }
-            float4 *d0 = reinterpret_cast<float4 *>(out + ((size_t)first * kD + r) * kD + 32 * q);
-            float4 *d1 = reinterpret_cast<float4 *>(out + ((size_t)last * kD + r) * kD + 32 * q);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float4 w = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-                d0[e] = w;
-                if (steps <= 0 && p.frames >= 2) d1[e] = w;  // no written frame: the far anchor keeps S_0
-            }
-            if (steps >= 1) form_u(v, al, sm.bf, r, q, t_hi, t_lo);
+            stage_row(sm, r, q, v);
+            if (steps >= 1) form_u(v, al, bn, q, t_hi, t_lo);
         }
+        // no written frame: the far anchor keeps S_0
+        write_rows(sm, r, out + (size_t)first * kD * kD,
+                   steps <= 0 && p.frames >= 2 ? out + (size_t)last * kD * kD : nullptr);
         ptx::tmem_st_wait();
     }
     ptx::tc_fence_before();
     ptx::mbar_arrive(sm.b(kBarA));
     for (int s = 1; ok && s <= steps; ++s) {
+        if (s < steps) fetch_b(s + 1);  // in flight while the MMAs run
         ok = __all_sync(0xffffffffu, wait_bar(sm, kBarD, (uint32_t)((s - 1) & 1), p, kWhereD));
         if (!ok) break;
         ptx::tc_fence_after();
@@ -821,10 +860,9 @@ __device__ void rows(const Params &p, const Smem &sm, uint32_t tmem, int h, int 
             if (!ok) break;
         }
         const int t = frame_of(p, dir, s);
-        const float *al = s < steps ? alpha_of(s + 1) : nullptr;
-        float *dst = out + ((size_t)t * kD + r) * kD;
-        float *dlast = out + ((size_t)last * kD + r) * kD;
-#pragma unroll 1
+        const float *al = sm.af;
+
+#pragma unroll
         for (int q = 0; q < 4; ++q) {
             uint32_t d[32];
             ptx::tmem_ld_32x32b_x32(t_d + (uint32_t)(32 * q), d);
@@ -833,14 +871,11 @@ __device__ void rows(const Params &p, const Smem &sm, uint32_t tmem, int h, int 
             float v[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(d[e]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float4 w = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-                reinterpret_cast<float4 *>(dst + 32 * q)[e] = w;
-                if (s == steps) reinterpret_cast<float4 *>(dlast + 32 * q)[e] = w;  // the far anchor frame
-            }
-            if (s < steps) form_u(v, al, sm.bf, r, q, t_hi, t_lo);
+            stage_row(sm, r, q, v);
+            if (s < steps) form_u(v, al, bn, q, t_hi, t_lo);
         }
+        // the last written state also goes to the far anchor frame
+        write_rows(sm, r, out + (size_t)t * kD * kD, s == steps ? out + (size_t)last * kD * kD : nullptr);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(sm.b(kBarA));
@@ -856,9 +891,10 @@ __global__ void __launch_bounds__(sc::kThreads, 1) vda_scan_tc_kernel(const sc::
     uint8_t *smem = smem_raw + (base - raw);
     sc::Smem sm;
     sm.m = base + sc::kSmemM;
-    sm.bq = base + sc::kSmemB;
+    sm.al = base + sc::kSmemAl;
+    sm.af = reinterpret_cast<const float *>(smem + sc::kSmemAl);
+    sm.stage = reinterpret_cast<float *>(smem + sc::kSmemStage);
     sm.bar = base + sc::kSmemBar;
-    sm.bf = reinterpret_cast<const float *>(smem + sc::kSmemB);
     sm.abort_flag = reinterpret_cast<volatile int *>(smem + sc::kSmemMisc + 4);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + sc::kSmemMisc);
     const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
