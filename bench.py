@@ -362,7 +362,7 @@ def run_fv(args):
             written = max(0, frames - 2)
             flops = w.heads * (written * (4.0 * t_f * dd * dd + 4.3 * dd ** 3 + 2 * 2.0 * dd ** 3)
                                + frames * 2.0 * t_f * dd * dd)
-            delta = {"kernels": "vda_stats_tc, vda_solve, vda_scan, vda_wsplit, vda_readout_tc", "ms": dms,
+            delta = {"kernels": "vda_stats_tc, vda_solve, vda_scan_tc, vda_wsplit, vda_readout_tc", "ms": dms,
                      "gflop": flops / 1e9, "tflops": flops / (dms / 1e3) / 1e12,
                      "vdn_hybrid_ms": (window["ms"] + dms) if window else None}
 
