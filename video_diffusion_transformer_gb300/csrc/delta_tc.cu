@@ -618,14 +618,15 @@ __global__ void __launch_bounds__(ro::kThreads, 1)
 // float32 accumulate; the dropped U_lo M_lo is below 2^-17 of the product).
 // B_t arrives transposed (float32) so that thread r reads row r of B_t
 // without bank conflicts.
-// 160 threads: warps 0-3 own the 128 state rows (TMEM lanes): they store
-// S_t = D, form U_{t+1} from it, alpha_{t+1} and B_{t+1}, and write its bf16
-// split; warp 4 (one thread) loads M (two buffers) and B (one buffer) by bulk
+// 288 threads: warps 0-7 own the 128 state rows (TMEM lanes), two threads a
+// row (warps w and w + 4 share lanes 32 (w % 4) .., columns 0-63 and 64-127):
+// they store S_t = D, form U_{t+1} from it, alpha_{t+1} and B_{t+1}, and write
+// its bf16 split; warp 8 (one thread) loads M (two buffers) and alpha by bulk
 // copy and issues the MMAs.
 namespace sc {
 
-constexpr int kThreads = 160;
-constexpr int kCtlWarp = 4;
+constexpr int kThreads = 288;
+constexpr int kCtlWarp = 8;
 constexpr uint32_t kTmemCols = 256;            // D (0-127), U_hi (128-191), U_lo (192-255)
 constexpr int kMBytes = 2 * 32768;             // M_t: hi and lo operand tiles
 constexpr int kABytes = kD * 4;                // alpha_t, float32
@@ -778,14 +779,14 @@ __device__ __forceinline__ void split_store(const float (&v)[32], uint32_t t_hi,
     ptx::tmem_st_32x32b_x16(t_lo + (uint32_t)(16 * q), lo);
 }
 
-// U = S Diag(alpha) + B for columns 32 q .. 32 q + 31 of the row (b: the
-// row of B), written as the bf16 split
-__device__ __forceinline__ void form_u(const float (&v)[32], const float *al, const float (&b)[kD], int q,
-                                       uint32_t t_hi, uint32_t t_lo) {
+// U = S Diag(alpha) + B for columns 32 qg .. 32 qg + 31 of the row (b: this
+// thread's half row of B, of which they are chunk q), written as the bf16 split
+__device__ __forceinline__ void form_u(const float (&v)[32], const float *al, const float (&b)[kD / 2], int q,
+                                       int qg, uint32_t t_hi, uint32_t t_lo) {
     float u[32];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) u[e] = fmaf(v[e], al[32 * q + e], b[32 * q + e]);
-    split_store(u, t_hi, t_lo, q);
+    for (int e = 0; e < 32; ++e) u[e] = fmaf(v[e], al[32 * qg + e], b[32 * q + e]);
+    split_store(u, t_hi, t_lo, qg);
 }
 
 // Stage columns 32 q .. 32 q + 31 of row r
@@ -795,33 +796,37 @@ __device__ __forceinline__ void stage_row(const Smem &sm, int r, int q, const fl
     for (int e = 0; e < 8; ++e) d[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
 }
 
-// The warp's 32 staged rows to frame rows of dst (and of dst2 when given):
-// one whole 512-byte row per store instruction
-__device__ __forceinline__ void write_rows(const Smem &sm, int r, float *dst, float *dst2) {
+// The warp's 32 staged half rows (columns 64 ch ..) to the frame's rows in
+// dst (and dst2 when given): two 256-byte half rows per store instruction
+__device__ __forceinline__ void write_rows(const Smem &sm, int r, int ch, float *dst, float *dst2) {
     __syncwarp();
     const int lane = r & 31, r0 = r & ~31;
+    const int c = 64 * ch + 4 * (lane & 15);
 #pragma unroll 4
-    for (int i = 0; i < 32; ++i) {
-        const float4 w = reinterpret_cast<const float4 *>(sm.stage + (size_t)(r0 + i) * kStageLd)[lane];
-        reinterpret_cast<float4 *>(dst + (size_t)(r0 + i) * kD)[lane] = w;
-        if (dst2 != nullptr) reinterpret_cast<float4 *>(dst2 + (size_t)(r0 + i) * kD)[lane] = w;
+    for (int i = 0; i < 16; ++i) {
+        const int row = r0 + 2 * i + (lane >> 4);
+        const float4 w = *reinterpret_cast<const float4 *>(sm.stage + (size_t)row * kStageLd + c);
+        *reinterpret_cast<float4 *>(dst + (size_t)row * kD + c) = w;
+        if (dst2 != nullptr) *reinterpret_cast<float4 *>(dst2 + (size_t)row * kD + c) = w;
     }
     __syncwarp();
 }
 
-__device__ void rows(const Params &p, const Smem &sm, uint32_t tmem, int h, int dir, int r) {
+__device__ void rows(const Params &p, const Smem &sm, uint32_t tmem, int h, int dir, int t) {
     const int steps = p.frames - 2;
+    const int r = ((t >> 5) & 3) * 32 + (t & 31);  // the row (TMEM lane)
+    const int ch = t >> 7;                          // the column half
     const uint32_t lane_base = (uint32_t)((r >> 5) * 32) << 16;
     const uint32_t t_d = tmem + lane_base, t_hi = tmem + lane_base + 128u, t_lo = tmem + lane_base + 192u;
     float *out = p.states + ((size_t)dir * p.heads + h) * (size_t)p.frames * kD * kD;
     const int first = frame_of(p, dir, 0), last = frame_of(p, dir, p.frames - 1);
-    // row r of B_k (B_k^T is stored, so a warp's loads are 128-byte
-    // segments), fetched into registers a step ahead of its use
-    float bn[kD];
+    // this thread's half row of B_k (B_k^T is stored, so a warp's loads are
+    // 128-byte segments), fetched into registers a step ahead of its use
+    float bn[kD / 2];
     auto fetch_b = [&](int step) {
         const float *src = p.ws_c + ((size_t)h * p.frames + frame_of(p, dir, step)) * kD * kD + r;
 #pragma unroll
-        for (int c = 0; c < kD; ++c) bn[c] = src[(size_t)c * kD];
+        for (int c = 0; c < kD / 2; ++c) bn[c] = src[(size_t)(64 * ch + c) * kD];
     };
     if (steps >= 1) fetch_b(1);
     // S_0: half the text state (or zero); U_1 from it
@@ -830,21 +835,22 @@ __device__ void rows(const Params &p, const Smem &sm, uint32_t tmem, int h, int 
     if (ok) {
         const float *al = sm.af;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
+            const int qg = 2 * ch + q;
             float v[32];
             if (p.text_state != nullptr) {
-                const float *src = p.text_state + ((size_t)h * kD + r) * kD + 32 * q;
+                const float *src = p.text_state + ((size_t)h * kD + r) * kD + 32 * qg;
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = 0.5f * src[e];
             } else {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = 0.0f;
             }
-            stage_row(sm, r, q, v);
-            if (steps >= 1) form_u(v, al, bn, q, t_hi, t_lo);
+            stage_row(sm, r, qg, v);
+            if (steps >= 1) form_u(v, al, bn, q, qg, t_hi, t_lo);
         }
         // no written frame: the far anchor keeps S_0
-        write_rows(sm, r, out + (size_t)first * kD * kD,
+        write_rows(sm, r, ch, out + (size_t)first * kD * kD,
                    steps <= 0 && p.frames >= 2 ? out + (size_t)last * kD * kD : nullptr);
         ptx::tmem_st_wait();
     }
@@ -859,23 +865,23 @@ __device__ void rows(const Params &p, const Smem &sm, uint32_t tmem, int h, int 
             ok = __all_sync(0xffffffffu, wait_bar(sm, kBarB, (uint32_t)(s & 1), p, kWhereB));
             if (!ok) break;
         }
-        const int t = frame_of(p, dir, s);
+        const int tf = frame_of(p, dir, s);
         const float *al = sm.af;
-
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
+            const int qg = 2 * ch + q;
             uint32_t d[32];
-            ptx::tmem_ld_32x32b_x32(t_d + (uint32_t)(32 * q), d);
+            ptx::tmem_ld_32x32b_x32(t_d + (uint32_t)(32 * qg), d);
             ptx::tmem_ld_wait();
             ptx::reg_fence(d);
             float v[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(d[e]);
-            stage_row(sm, r, q, v);
-            if (s < steps) form_u(v, al, bn, q, t_hi, t_lo);
+            stage_row(sm, r, qg, v);
+            if (s < steps) form_u(v, al, bn, q, qg, t_hi, t_lo);
         }
         // the last written state also goes to the far anchor frame
-        write_rows(sm, r, out + (size_t)t * kD * kD, s == steps ? out + (size_t)last * kD * kD : nullptr);
+        write_rows(sm, r, ch, out + (size_t)tf * kD * kD, s == steps ? out + (size_t)last * kD * kD : nullptr);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(sm.b(kBarA));
@@ -904,7 +910,7 @@ __global__ void __launch_bounds__(sc::kThreads, 1) vda_scan_tc_kernel(const sc::
         ptx::mbar_init(sm.b(sc::kBarM + 1), 1);
         ptx::mbar_init(sm.b(sc::kBarB), 1);
         ptx::mbar_init(sm.b(sc::kBarD), 1);
-        ptx::mbar_init(sm.b(sc::kBarA), 128);
+        ptx::mbar_init(sm.b(sc::kBarA), 256);
         *sm.abort_flag = 0;
         ptx::fence_barrier_init();
     }
