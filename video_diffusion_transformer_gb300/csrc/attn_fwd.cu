@@ -21,10 +21,11 @@
 //     tensor core works on one tile while the other tile's softmax runs;
 //   * warps 0-3 and 4-7 are the softmax warpgroups of q-tile 0 and 1: thread
 //     t owns query row t (TMEM lane t).  Per K/V tile it reads its 128 scores
-//     from TMEM, takes the row maximum, writes p = 2^(s*scale*log2e - m) as
-//     bf16 back over the scores, and adds p to its float32 row sum.  The
-//     running maximum is raised (and O rescaled in TMEM) only when the tile
-//     maximum exceeds it by more than 2^8, so rescaling is rare;
+//     from TMEM, writes p = 2^(s*scale*log2e - m) as bf16 back over the
+//     scores, and adds p to its float32 row sum.  m is the row maximum of the
+//     unit's first tile; a later tile takes its own maximum (and O is
+//     rescaled in TMEM) only when its probabilities sum above 2^20, so there
+//     is no per-tile maximum on the critical path and rescaling is rare;
 //   * TMEM (512 columns): S_0, S_1 at columns 0 and 128, O_0, O_1 at 256 and
 //     384, each 128 lanes x 128 float32 columns.  P_k (bf16 pairs) overwrites
 //     the first 64 columns of S_k.
