@@ -358,30 +358,37 @@ namespace ro {
 constexpr int kRows = 128;
 constexpr int kBox = kRows * 64 * 2;          // 128 rows x 64 channels (16 KB)
 constexpr int kTile = 2 * kBox;               // 32 KB
-constexpr int kOffQ = 0, kOffWHi = kTile, kOffWLo = 2 * kTile;
-constexpr int kStageBytes = 3 * kTile;        // 96 KB
-constexpr int kStages = 2;
+constexpr int kOffWHi = 0, kOffWLo = kTile;   // the item's W split, resident
+constexpr int kOffQ = 2 * kTile;              // Q ring
+constexpr int kQStages = 3;
+constexpr int kParts = 4;                     // row-tile runs per (chunk, head)
+constexpr int kOutLd = 272;                   // staged output row: 256 bytes + 16 (conflict-free)
 constexpr int kThreads = 192;
 constexpr int kTmaWarp = 4, kMmaWarp = 5;
 constexpr uint32_t kTmemCols = 256;
 
-constexpr int kBarFull = 0;                   // TMA -> MMA and epilogue
-constexpr int kBarEmpty = kBarFull + kStages; // MMA commit + 128 epilogue arrivals -> producer
-constexpr int kBarAccFull = kBarEmpty + kStages;
+constexpr int kBarFull = 0;                   // Q slot loaded (TMA -> MMA and epilogue)
+constexpr int kBarEmpty = kBarFull + kQStages;  // MMA commit + 128 epilogue arrivals -> producer
+constexpr int kBarWFull = kBarEmpty + kQStages; // the item's W loaded
+constexpr int kBarWEmpty = kBarWFull + 1;     // the item's MMAs done
+constexpr int kBarAccFull = kBarWEmpty + 1;
 constexpr int kBarAccEmpty = kBarAccFull + 2;
 constexpr int kBarDrain = kBarAccEmpty + 2;
 constexpr int kNumBars = kBarDrain + 1;
-constexpr int kSmemBar = kStages * kStageBytes;
+
+constexpr int kOffOut = kOffQ + kQStages * kTile;  // [128 rows][kOutLd bytes] bf16 output
+constexpr int kSmemBar = kOffOut + kRows * kOutLd;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
 constexpr int kSmemBytes = kSmemMisc + 16 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
-constexpr int kWhereEmpty = 1, kWhereFull = 2, kWhereAccEmpty = 3, kWhereAccFull = 4, kWhereDrain = 5;
+constexpr int kWhereEmpty = 1, kWhereFull = 2, kWhereAccEmpty = 3, kWhereAccFull = 4, kWhereDrain = 5,
+              kWhereWEmpty = 6, kWhereWFull = 7;
 
 struct Params {
     __nv_bfloat16 *o;
     int *status;
-    int n, ld, heads, chunk_tokens, chunks, tiles_per_chunk, num_units;
+    int n, ld, heads, chunk_tokens, chunks, tiles_per_chunk, tiles_per_part, num_items;
 };
 
 struct Smem {
@@ -399,70 +406,103 @@ __device__ __forceinline__ void drain_bar(const Smem &sm, int i, uint32_t parity
     ptx::mbar_wait(sm.b(i), parity, &never, p.status, kDevTimeout | kWhereDrain);
 }
 
-struct Unit {
-    int head, chunk, row0, row_end;  // rows [row0, min(row0 + 128, row_end)) are stored
+// Work item = (chunk, head, part): row tiles [t0, t1) of the chunk, read
+// against the one W split of (chunk, head), which stays in shared memory for
+// the whole run.  Parts innermost, then heads, so the CTAs running together
+// read nearby Q rows.
+struct Item {
+    int head, chunk, t0, t1, row_end;
 };
 
-__device__ __forceinline__ Unit unit_of(const Params &p, int unit) {
-    Unit u;
-    u.head = unit % p.heads;
-    const int tile = unit / p.heads;
-    u.chunk = tile / p.tiles_per_chunk;
-    u.row0 = u.chunk * p.chunk_tokens + (tile % p.tiles_per_chunk) * kRows;
-    u.row_end = min(p.n, (u.chunk + 1) * p.chunk_tokens);
-    return u;
+__device__ __forceinline__ Item item_of(const Params &p, int i) {
+    Item it;
+    const int part = i % kParts;
+    it.head = (i / kParts) % p.heads;
+    it.chunk = i / (kParts * p.heads);
+    it.t0 = part * p.tiles_per_part;
+    it.t1 = min(p.tiles_per_chunk, it.t0 + p.tiles_per_part);
+    it.row_end = min(p.n, (it.chunk + 1) * p.chunk_tokens);
+    return it;
+}
+
+// first row of row tile `tile` of the item's chunk
+__device__ __forceinline__ int tile_row0(const Params &p, const Item &it, int tile) {
+    return it.chunk * p.chunk_tokens + tile * kRows;
 }
 
 __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tw, const Params &p, const Smem &sm) {
-    uint32_t g = 0;
+    uint32_t g = 0, w = 0;  // Q tiles and W splits loaded
     bool ok = true;
-    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x, ++g) {
-        const Unit u = unit_of(p, unit);
-        const uint32_t slot = g % kStages;
-        ok = wait_bar(sm, kBarEmpty + (int)slot, ((g / kStages) & 1u) ^ 1u, p, kWhereEmpty);
+    for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x) {
+        const Item it = item_of(p, i);
+        if (it.t0 >= it.t1) continue;
+        // the previous item's MMAs are done with W
+        ok = wait_bar(sm, kBarWEmpty, (w & 1u) ^ 1u, p, kWhereWEmpty);
         if (!ok) break;
-        const uint32_t base = sm.stages + slot * (uint32_t)kStageBytes;
-        const uint32_t bar = sm.b(kBarFull + (int)slot);
-        ptx::mbar_arrive_expect_tx(bar, kStageBytes);
-        const int wrow = (u.head * p.chunks + u.chunk) * 2 * kRows;
-        for (int c = 0; c < 2; ++c) {
-            ptx::tma_load_2d(base + kOffQ + c * kBox, tq, bar, u.head * 128 + 64 * c, u.row0);
-            ptx::tma_load_2d(base + kOffWHi + c * kBox, tw, bar, 64 * c, wrow);
-            ptx::tma_load_2d(base + kOffWLo + c * kBox, tw, bar, 64 * c, wrow + kRows);
+        {
+            const uint32_t bar = sm.b(kBarWFull);
+            ptx::mbar_arrive_expect_tx(bar, 2 * kTile);
+            const int wrow = (it.head * p.chunks + it.chunk) * 2 * kRows;
+            for (int c = 0; c < 2; ++c) {
+                ptx::tma_load_2d(sm.stages + kOffWHi + c * kBox, tw, bar, 64 * c, wrow);
+                ptx::tma_load_2d(sm.stages + kOffWLo + c * kBox, tw, bar, 64 * c, wrow + kRows);
+            }
+            ++w;
+        }
+        for (int tile = it.t0; ok && tile < it.t1; ++tile, ++g) {
+            const uint32_t slot = g % kQStages;
+            ok = wait_bar(sm, kBarEmpty + (int)slot, ((g / kQStages) & 1u) ^ 1u, p, kWhereEmpty);
+            if (!ok) break;
+            const uint32_t dst = sm.stages + kOffQ + slot * (uint32_t)kTile;
+            const uint32_t bar = sm.b(kBarFull + (int)slot);
+            ptx::mbar_arrive_expect_tx(bar, kTile);
+            for (int c = 0; c < 2; ++c)
+                ptx::tma_load_2d(dst + c * kBox, tq, bar, it.head * 128 + 64 * c, tile_row0(p, it, tile));
         }
     }
-    for (uint32_t i = 0; i < (uint32_t)kStages && i < g; ++i) {
-        const uint32_t last = g - 1u - i;
-        drain_bar(sm, kBarFull + (int)(last % kStages), (last / kStages) & 1u, p);
+    // every copy issued must have landed before the CTA exits
+    for (uint32_t k = 0; k < (uint32_t)kQStages && k < g; ++k) {
+        const uint32_t last = g - 1u - k;
+        drain_bar(sm, kBarFull + (int)(last % kQStages), (last / kQStages) & 1u, p);
     }
+    if (w > 0) drain_bar(sm, kBarWFull, (w - 1u) & 1u, p);
 }
 
-constexpr uint64_t kDescStage = (uint64_t)(kStageBytes >> 4);
+constexpr uint64_t kDescTile = (uint64_t)(kTile >> 4);
 
 __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
     const uint64_t dq = ptx::sdesc_sw128(sm.stages + kOffQ, 16, 1024);
     const uint64_t dwh = ptx::sdesc_sw128(sm.stages + kOffWHi, 16, 1024);
     const uint64_t dwl = ptx::sdesc_sw128(sm.stages + kOffWLo, 16, 1024);
     constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
-    uint32_t g = 0;
+    uint32_t g = 0, w = 0;
     bool ok = true;
-    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x, ++g) {
-        const uint32_t slot = g % kStages, buf = g & 1u;
-        ok = wait_bar(sm, kBarAccEmpty + (int)buf, ((g >> 1) & 1u) ^ 1u, p, kWhereAccEmpty);
+    for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x) {
+        const Item it = item_of(p, i);
+        if (it.t0 >= it.t1) continue;
+        ok = wait_bar(sm, kBarWFull, w & 1u, p, kWhereWFull);
         if (!ok) break;
-        ok = wait_bar(sm, kBarFull + (int)slot, (g / kStages) & 1u, p, kWhereFull);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        const uint64_t so = slot * kDescStage;
-        const uint32_t d = tmem + 128u * buf;
+        ++w;
+        for (int tile = it.t0; ok && tile < it.t1; ++tile, ++g) {
+            const uint32_t slot = g % kQStages, buf = g & 1u;
+            ok = wait_bar(sm, kBarAccEmpty + (int)buf, ((g >> 1) & 1u) ^ 1u, p, kWhereAccEmpty);
+            if (!ok) break;
+            ok = wait_bar(sm, kBarFull + (int)slot, (g / kQStages) & 1u, p, kWhereFull);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint64_t qs = slot * kDescTile;
+            const uint32_t d = tmem + 128u * buf;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t off = so + (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
-            ptx::mma_ss(d, dq + off, dwh + off, idesc, kk > 0 ? 1u : 0u);
-            ptx::mma_ss(d, dq + off, dwl + off, idesc, 1u);
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
+                ptx::mma_ss(d, dq + qs + off, dwh + off, idesc, kk > 0 ? 1u : 0u);
+                ptx::mma_ss(d, dq + qs + off, dwl + off, idesc, 1u);
+            }
+            ptx::tc_commit(sm.b(kBarEmpty + (int)slot));
+            ptx::tc_commit(sm.b(kBarAccFull + (int)buf));
         }
-        ptx::tc_commit(sm.b(kBarEmpty + (int)slot));
-        ptx::tc_commit(sm.b(kBarAccFull + (int)buf));
+        if (!ok) break;
+        ptx::tc_commit(sm.b(kBarWEmpty));  // W may be replaced once these MMAs are done
     }
     ptx::tc_commit(sm.b(kBarDrain));
     drain_bar(sm, kBarDrain, 0u, p);
@@ -473,18 +513,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ void epilogue(const Params &p, const Smem &sm, const uint8_t *smem_stages, uint32_t tmem, int t) {
+__device__ void epilogue(const Params &p, const Smem &sm, uint8_t *smem_stages, uint32_t tmem, int t) {
     const uint32_t lane_base = (uint32_t)((t >> 5) * 32) << 16;
     uint32_t g = 0;
     bool ok = true;
-    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x, ++g) {
-        const Unit u = unit_of(p, unit);
-        const uint32_t slot = g % kStages, buf = g & 1u;
-        ok = __all_sync(0xffffffffu, wait_bar(sm, kBarFull + (int)slot, (g / kStages) & 1u, p, kWhereFull));
+    for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x) {
+      const Item it = item_of(p, i);
+      for (int tile = it.t0; ok && tile < it.t1; ++tile, ++g) {
+        const uint32_t slot = g % kQStages, buf = g & 1u;
+        ok = __all_sync(0xffffffffu, wait_bar(sm, kBarFull + (int)slot, (g / kQStages) & 1u, p, kWhereFull));
         if (!ok) break;
         // |q| of row t: its 16 chunks of 16 bytes, in any order (the sum does
         // not care about the swizzle), from a lane-dependent start
-        const uint8_t *qrow = smem_stages + (size_t)slot * kStageBytes + kOffQ + t * 128;
+        const uint8_t *qrow = smem_stages + kOffQ + (size_t)slot * kTile + t * 128;
         float ss = 0.f;
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -502,29 +543,40 @@ __device__ void epilogue(const Params &p, const Smem &sm, const uint8_t *smem_st
         ok = __all_sync(0xffffffffu, wait_bar(sm, kBarAccFull + (int)buf, (g >> 1) & 1u, p, kWhereAccFull));
         if (!ok) break;
         ptx::tc_fence_after();
-        const int row = u.row0 + t;
-        const bool row_ok = row < u.row_end;
-        uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(row_ok ? row : 0) * (size_t)p.ld + (size_t)u.head * 128);
+        uint8_t *stage = smem_stages + kOffOut;
 #pragma unroll 1
         for (int c4 = 0; c4 < 4; ++c4) {
             uint32_t r[32];
             ptx::tmem_ld_32x32b_x32(tmem + lane_base + 128u * buf + 32u * (uint32_t)c4, r);
             ptx::tmem_ld_wait();
             ptx::reg_fence(r);
-            if (row_ok) {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
-                    w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
-                    w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
-                    w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
-                    dst[c4 * 4 + v] = w;
-                }
+            for (int v = 0; v < 4; ++v) {
+                uint4 w;
+                w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
+                w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
+                w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
+                w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
+                *reinterpret_cast<uint4 *>(stage + t * kOutLd + (c4 * 4 + v) * 16) = w;
             }
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(sm.b(kBarAccEmpty + (int)buf));
+        // the warp's 32 rows out, two whole 256-byte rows per store instruction
+        __syncwarp();
+        {
+            const int lane = t & 31, r0 = t & ~31;
+#pragma unroll 4
+            for (int k = 0; k < 16; ++k) {
+                const int rr = r0 + 2 * k + (lane >> 4), ch = lane & 15;
+                const int orow = tile_row0(p, it, tile) + rr;
+                const uint4 w = *reinterpret_cast<const uint4 *>(stage + rr * kOutLd + ch * 16);
+                if (orow < it.row_end)
+                    reinterpret_cast<uint4 *>(p.o + (size_t)orow * (size_t)p.ld + (size_t)it.head * 128)[ch] = w;
+            }
+        }
+        __syncwarp();
+      }
     }
 }
 
@@ -567,10 +619,12 @@ __global__ void __launch_bounds__(ro::kThreads, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + ro::kSmemMisc);
     const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < ro::kStages; ++s) {
+        for (int s = 0; s < ro::kQStages; ++s) {
             ptx::mbar_init(sm.b(ro::kBarFull + s), 1);
             ptx::mbar_init(sm.b(ro::kBarEmpty + s), 1 + 128);
         }
+        ptx::mbar_init(sm.b(ro::kBarWFull), 1);
+        ptx::mbar_init(sm.b(ro::kBarWEmpty), 1);
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(sm.b(ro::kBarAccFull + b), 1);
             ptx::mbar_init(sm.b(ro::kBarAccEmpty + b), 128);
@@ -1046,10 +1100,11 @@ fv_status launch_vda_readout_tc(const DeltaLaunch &a, __nv_bfloat16 *wsplit, cud
     p.chunk_tokens = a.chunk_frames * a.frame_tokens;
     p.chunks = chunks;
     p.tiles_per_chunk = (p.chunk_tokens + ro::kRows - 1) / ro::kRows;
+    p.tiles_per_part = (p.tiles_per_chunk + ro::kParts - 1) / ro::kParts;
     // every chunk but the last holds chunk_tokens rows; the last one's extra
     // tiles (past the sequence) are still dealt out and store nothing
-    p.num_units = chunks * p.tiles_per_chunk * a.heads;
-    const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
+    p.num_items = chunks * a.heads * ro::kParts;
+    const int grid = p.num_items < a.num_sms ? p.num_items : a.num_sms;
     vda_readout_tc_kernel<<<grid, ro::kThreads, ro::kSmemBytes, stream>>>(mq, mw, p);
     return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
 }
