@@ -19,8 +19,9 @@
 //     (w_A K)_lo, D_B += (w_B V)_hi^T K, D_B += (w_B V)_lo^T K, both operands
 //     MN-major (channels contiguous); D_A and D_B in tensor memory, double
 //     buffered across units;
-//   warps 0-3 (the epilogue): thread = row i of D; writes row i of I + A_t and
-//     column i of B_t^T (float32) to the workspace.
+//   warps 0-3 (the epilogue): thread = row i of D; writes it as column i of
+//     I + A_t (symmetric) and of B_t^T (float32) to the workspace, so a
+//     warp's stores are 128-byte segments.
 // All waits are bounded; a wait that runs out records kDevTimeout | where.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -249,9 +250,11 @@ __device__ void epilogue(const Params &p, const Smem &sm, uint32_t tmem, int t) 
         ok = __all_sync(0xffffffffu, wait_bar(sm, kBarAccFull + (int)buf, (units >> 1) & 1u, p, kWhereAccFull));
         if (!ok) break;
         ptx::tc_fence_after();
-        const size_t base = (((size_t)head * p.frames + frame) * kD + t) * kD;
+        // Row t of D goes out as column t (a warp's 32 rows form one 128-byte
+        // segment per column): B_t^T for the scan, and I + A_t, which is
+        // symmetric, so its transpose is itself.
         for (int m = 0; m < 2; ++m) {
-            float *dst = (m == 0 ? p.ws_m : p.ws_c) + base;
+            float *col = (m == 0 ? p.ws_m : p.ws_c) + ((size_t)head * p.frames + frame) * kD * kD + t;
 #pragma unroll 1
             for (int c4 = 0; c4 < 4; ++c4) {
                 uint32_t r[32];
@@ -263,18 +266,8 @@ __device__ void epilogue(const Params &p, const Smem &sm, uint32_t tmem, int t) 
                     for (int e = 0; e < 32; ++e)
                         if (e == (t & 31)) r[e] = __float_as_uint(__uint_as_float(r[e]) + 1.0f);
                 }
-                if (m == 0) {
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        *reinterpret_cast<uint4 *>(dst + 32 * c4 + 4 * v) =
-                            make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-                } else {
-                    // B_t transposed: column c of B is row c of ws_c (the
-                    // warp's 32 rows t form one 128-byte segment)
-                    float *bt = p.ws_c + ((size_t)head * p.frames + frame) * kD * kD + t;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) bt[(size_t)(32 * c4 + e) * kD] = __uint_as_float(r[e]);
-                }
+                for (int e = 0; e < 32; ++e) col[(size_t)(32 * c4 + e) * kD] = __uint_as_float(r[e]);
             }
         }
         ptx::tc_fence_before();
