@@ -131,16 +131,19 @@ def test_ten_second_clip_grid():
 
 
 @pytest.mark.parametrize("hot_tile", [1, 5, 10])
-def test_large_scores_late_in_the_list(hot_tile):
-    """Keys of one tile scaled by 16: with every tile kept, its scores exceed
-    the running maximum by far when it is reached, in the second half of the
-    first K/V tile (tile 1), or later (tiles 5, 10), so the kernel must
-    rescale the probabilities and the output it already holds."""
+@pytest.mark.parametrize("gain", [6, 16])
+def test_large_scores_late_in_the_list(hot_tile, gain):
+    """Keys of one tile scaled up: with every tile kept, its scores exceed the
+    running maximum when it is reached, in the second half of the first K/V
+    tile (tile 1) or later (tiles 5, 10).  Gain 6 leaves most late halves
+    within the kernel's 2^20 bound against the first maximum (summed as they
+    are); gain 16 takes them past it, so the kernel must rescale the
+    probabilities and the output it already holds."""
     grid, heads = (8, 8, 12), 2
     n = grid[0] * grid[1] * grid[2]
     q, k, v = rand(n, heads, 40 + hot_tile)
     idx = VS.tile_tokens(*grid)[hot_tile]
-    k[idx] = (k[idx].float() * 16).to(torch.bfloat16)
+    k[idx] = (k[idx].float() * gain).to(torch.bfloat16)
     check(q, k, v, grid, fv.vsa_num_tiles(*grid))
 
 

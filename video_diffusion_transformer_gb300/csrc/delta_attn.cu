@@ -36,6 +36,16 @@ constexpr int kDv = 128;          // key and value dimension of a head
 constexpr int kDThreads = 256;    // 16 x 16 threads, each an 8 x 8 block of a 128 x 128 result
 constexpr size_t kMat = (size_t)kDv * kDv;
 
+// (c0, c1) = (a0, a1) * b + (c0, c1): one packed instruction (sm_100+), each
+// lane rounded as a single fmaf.
+__device__ __forceinline__ void fma2_acc(float &c0, float &c1, float a0, float a1, float b) {
+    asm("{\n\t.reg .b64 a, b, c;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %4};\n\tmov.b64 c, {%0, %1};\n\t"
+        "fma.rn.f32x2 c, a, b, c;\n\tmov.b64 {%0, %1}, c;\n\t}"
+        : "+f"(c0), "+f"(c1)
+        : "f"(a0), "f"(a1), "f"(b));
+}
+
 
 // ------------------------------------------------------------------ solve
 // Gauss-Jordan inversion of G = I + A_t of frame t of head h in place:
@@ -105,10 +115,11 @@ __global__ void __launch_bounds__(kDThreads, 2) vda_solve_kernel(int frames, flo
                 for (int i = 0; i < 8; ++i) g[i][kk] = (own_row && i == kk) ? 1.0f : 0.0f;
             }
             if (own_row) f[kk] -= 1.0f;
+            // two elements per packed fma (each lane rounds as fmaf would)
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) g[i][j] = fmaf(-f[i], rg[j], g[i][j]);
+                for (int j = 0; j < 8; j += 2) fma2_acc(g[i][j], g[i][j + 1], rg[j], rg[j + 1], -f[i]);
         }
     }
     uint8_t *mo = reinterpret_cast<uint8_t *>(ws_m + base);
