@@ -12,15 +12,16 @@
 //             softmax window and n = (c + W + 1) C (clamped to F-1) the first
 //             frame after it.
 //
-// Four kernels:
+// Five kernels:
 //   stats   (frame, head; tensor cores, delta_tc.cu): I + A_t -> ws_m, B_t^T -> ws_c
 //   solve   (frame, head; float32): Gauss-Jordan inversion of I + A_t in registers,
 //           M_t = (I + A_t)^{-1} -> ws_m as bf16 hi/lo operand tiles
 //   scan    (head, direction; tensor cores, delta_tc.cu): S <- U M_t with
 //           U = S Diag(alpha_t) + B_t, frame by frame, split-bf16 products
 //           with float32 accumulation
-//   readout (chunk rows, head; tensor cores, delta_tc.cu): o = (S_fwd[p] + S_rev[n]) q_hat,
-//           rounded to bf16
+//   wsplit  (chunk, head; delta_tc.cu): W = S_fwd[p] + S_rev[n] as bf16 hi + lo
+//   readout (chunk rows, head; tensor cores, delta_tc.cu): o = W q_hat, rounded
+//           to bf16
 // The scan is the only sequential part: 2 H chains of F - 2 128x128x128 steps.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

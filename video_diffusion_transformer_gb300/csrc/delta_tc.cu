@@ -8,14 +8,14 @@
 // parts (x = hi + lo to about 2^-16 relative), so two bf16 MMAs with float32
 // accumulation give the sums to about float32 accuracy.
 //
-// vda_stats_tc (persistent, one CTA per SM, 320 threads): unit = (frame, head).
-//   warp 8 (one thread): TMA loads of 64-token stages, K and V as 64 x 64
+// vda_stats_tc (persistent, one CTA per SM, 448 threads): unit = (frame, head).
+//   warp 12 (one thread): TMA loads of 64-token stages, K and V as 64 x 64
 //     bf16 boxes in the 128-byte swizzled layout, two stages in flight;
-//   warps 4-7 (the scalers): thread = (token, channel half); squared norm of
-//     k over both halves, then w_A k and w_B v split into hi and lo, written
-//     to the same (swizzled) byte positions of their own buffers (v's hi
-//     over v itself), so every operand shares K's layout;
-//   warp 9 (one thread): per 16 tokens, D_A += K^T (w_A K)_hi, D_A += K^T
+//   warps 4-11 (the scalers): thread = (token, channel quarter); squared norm
+//     of k over the four quarters, then w_A k and w_B v split into hi and lo,
+//     written to the same (swizzled) byte positions of their own buffers (v's
+//     hi over v itself), so every operand shares K's layout;
+//   warp 13 (one thread): per 16 tokens, D_A += K^T (w_A K)_hi, D_A += K^T
 //     (w_A K)_lo, D_B += (w_B V)_hi^T K, D_B += (w_B V)_lo^T K, both operands
 //     MN-major (channels contiguous); D_A and D_B in tensor memory, double
 //     buffered across units;
@@ -44,12 +44,13 @@ constexpr int kOperand = 2 * kHalf;            // 64 tokens x 128 channels (16 K
 constexpr int kOffK = 0, kOffVHi = kOperand, kOffVLo = 2 * kOperand, kOffXHi = 3 * kOperand, kOffXLo = 4 * kOperand;
 constexpr int kStageBytes = 5 * kOperand;      // 80 KB
 constexpr int kStages = 2;
-constexpr int kThreads = 320;
-constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 448;
+constexpr int kScalers = 256;                  // warps 4-11: 64 tokens x 4 channel quarters
+constexpr int kTmaWarp = 12, kMmaWarp = 13;
 constexpr uint32_t kTmemCols = 512;            // 2 buffers x (D_A, D_B)
 
 constexpr int kBarKvFull = 0;                  // TMA -> scalers
-constexpr int kBarXFull = kBarKvFull + kStages;     // scalers -> MMA (128 arrivals)
+constexpr int kBarXFull = kBarKvFull + kStages;     // scalers -> MMA (256 arrivals)
 constexpr int kBarStageEmpty = kBarXFull + kStages;  // MMA -> producer
 constexpr int kBarAccFull = kBarStageEmpty + kStages;  // MMA -> epilogue
 constexpr int kBarAccEmpty = kBarAccFull + 2;  // epilogue -> MMA (128 arrivals)
@@ -127,9 +128,25 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bflo
     lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
-// Scaler thread t (0..127): token u = t / 2 of the stage, channel half c = t % 2.
+// (x0, x1) -> bf16 pairs hi and lo with x = hi + lo to about 2^-16 relative
+// (each part rounded to nearest), two lanes per conversion.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+// Scaler thread t (0..255): token u = t / 4 of the stage, channel quarter
+// c = t % 4, i.e. four of the eight 16-byte chunk positions of one half row
+// (half c / 2, positions 4 (c % 2) ..).  A thread visits its positions from
+// an offset that makes the eight lanes of a quarter-warp (two tokens, four
+// quarters) read eight different positions, i.e. eight bank groups.  The
+// swizzle does not matter here: a position is read and written in place.
 __device__ void scaler(const Params &p, const Smem &sm, uint8_t *smem_stages, int t) {
-    const int u = t >> 1, c = t & 1;
+    const int u = t >> 2, c = t & 3;
+    const int rot = 2 * (c >> 1) + u;
     uint32_t g = 0;
     bool ok = true;
     for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
@@ -144,49 +161,43 @@ __device__ void scaler(const Params &p, const Smem &sm, uint8_t *smem_stages, in
             ok = __all_sync(0xffffffffu, wait_bar(sm, kBarKvFull + (int)slot, (g / kStages) & 1u, p, kWhereKvFull));
             if (!ok) break;
             uint8_t *st = smem_stages + (size_t)slot * kStageBytes;
-            const int row_off = c * kHalf + u * 128;
-            // the row's eight 16-byte chunks, visited from a lane-dependent
-            // start so the eight lanes of a quarter-warp hit eight banks groups
-            uint4 kc[8];
+            const int row_off = (c >> 1) * kHalf + u * 128;
+            uint4 kc[4];
             float ss = 0.f;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int pos = (q + t) & 7;
-                kc[q] = *reinterpret_cast<const uint4 *>(st + kOffK + row_off + pos * 16);
-                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&kc[q]);
+            for (int i = 0; i < 4; ++i) {
+                const int pos = 4 * (c & 1) + ((i + rot) & 3);
+                kc[i] = *reinterpret_cast<const uint4 *>(st + kOffK + row_off + pos * 16);
+                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&kc[i]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 f = __bfloat1622float2(h2[e]);
                     ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
                 }
             }
-            ss += __shfl_xor_sync(0xffffffffu, ss, 1);  // the other channel half of the token
+            // the token's other three quarters
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
             const float wa = beta / fmaxf(ss, 1e-24f);
             const float wb = beta / fmaxf(sqrtf(ss), 1e-12f);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int pos = (q + t) & 7;
+            for (int i = 0; i < 4; ++i) {
+                const int pos = 4 * (c & 1) + ((i + rot) & 3);
                 const int off = row_off + pos * 16;
-                const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kc[q]);
+                const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kc[i]);
                 const uint4 vc = *reinterpret_cast<const uint4 *>(st + kOffVHi + off);
                 const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&vc);
-                uint4 xh, xl, vh, vl;
-                __nv_bfloat16 *xh_ = reinterpret_cast<__nv_bfloat16 *>(&xh);
-                __nv_bfloat16 *xl_ = reinterpret_cast<__nv_bfloat16 *>(&xl);
-                __nv_bfloat16 *vh_ = reinterpret_cast<__nv_bfloat16 *>(&vh);
-                __nv_bfloat16 *vl_ = reinterpret_cast<__nv_bfloat16 *>(&vl);
+                uint32_t xh[4], xl[4], vh[4], vl[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 kf = __bfloat1622float2(k2[e]), vf = __bfloat1622float2(v2[e]);
-                    split_bf16(wa * kf.x, xh_[2 * e], xl_[2 * e]);
-                    split_bf16(wa * kf.y, xh_[2 * e + 1], xl_[2 * e + 1]);
-                    split_bf16(wb * vf.x, vh_[2 * e], vl_[2 * e]);
-                    split_bf16(wb * vf.y, vh_[2 * e + 1], vl_[2 * e + 1]);
+                    split2(wa * kf.x, wa * kf.y, xh[e], xl[e]);
+                    split2(wb * vf.x, wb * vf.y, vh[e], vl[e]);
                 }
-                *reinterpret_cast<uint4 *>(st + kOffXHi + off) = xh;
-                *reinterpret_cast<uint4 *>(st + kOffXLo + off) = xl;
-                *reinterpret_cast<uint4 *>(st + kOffVHi + off) = vh;
-                *reinterpret_cast<uint4 *>(st + kOffVLo + off) = vl;
+                *reinterpret_cast<uint4 *>(st + kOffXHi + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+                *reinterpret_cast<uint4 *>(st + kOffXLo + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
+                *reinterpret_cast<uint4 *>(st + kOffVHi + off) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
+                *reinterpret_cast<uint4 *>(st + kOffVLo + off) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
             }
             // the tensor core reads these through the async proxy
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -291,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(sm.b(kBarKvFull + s), 1);
-            ptx::mbar_init(sm.b(kBarXFull + s), 128);
+            ptx::mbar_init(sm.b(kBarXFull + s), kScalers);
             ptx::mbar_init(sm.b(kBarStageEmpty + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
