@@ -433,10 +433,19 @@ def run_fv(args):
                     times.append(e0.elapsed_time(e1))
                 return statistics.median(times), min(times)
 
+            # per-token modality rows: three modalities (row step * 3 + tag),
+            # tags drawn per token (the most mixed packing)
+            nmod = 3
+            tags = torch.randint(0, nmod, (rows,), generator=ge, device=dev, dtype=torch.int64).to(torch.uint8)
+            shift_t, scale_t, gate_t = (t.repeat_interleave(nmod, dim=0).contiguous() for t in (shift, scale, gate))
             with torch.cuda.stream(stream):
                 mod = time_reps(lambda: fv.adaln_modulate(ex, shift, scale, W.ADALN_STEP, eps=EPS, out=ey,
                                                           stream=stream))
                 gre = time_reps(lambda: fv.gated_residual(ex, ea, gate, W.ADALN_STEP, out=eo, stream=stream))
+                mod_t = time_reps(lambda: fv.adaln_modulate_tagged(ex, shift_t, scale_t, W.ADALN_STEP, tags, nmod,
+                                                                   eps=EPS, out=ey, stream=stream))
+                gre_t = time_reps(lambda: fv.gated_residual_tagged(ex, ea, gate_t, W.ADALN_STEP, tags, nmod, out=eo,
+                                                                   stream=stream))
             fv.sync_status(stream)
             mod_bytes = rows * W.HIDDEN * 4 + 2 * W.HIDDEN * 4
             gre_bytes = rows * W.HIDDEN * 6 + W.HIDDEN * 4
@@ -449,8 +458,13 @@ def run_fv(args):
 
             elementwise = {"rows": rows, "hidden": W.HIDDEN, "flush": "512 MB written before every rep",
                            "reps": 20, "peak_gbs": hbm, "adaln_modulate_bf16": entry(mod, mod_bytes),
-                           "gated_residual": entry(gre, gre_bytes)}
-            del ex, ea, ey, eo, flush
+                           "gated_residual": entry(gre, gre_bytes),
+                           "tagged": {"modalities": nmod, "tags": "one per token, seeded uniform",
+                                      "adaln_modulate_bf16": entry(mod_t, rows * W.HIDDEN * 4 + rows
+                                                                   + nmod * 2 * W.HIDDEN * 4),
+                                      "gated_residual": entry(gre_t, rows * W.HIDDEN * 6 + rows
+                                                              + nmod * W.HIDDEN * 4)}}
+            del ex, ea, ey, eo, flush, tags
 
         # ---- end to end through the C ABI: pinned host inputs in, results out.
         # Every step copies its own inputs host->device and reads its results

@@ -10,6 +10,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "fv_internal.h"
 
 namespace fv {
@@ -56,6 +58,73 @@ __device__ __forceinline__ float warp_sum(float v) {
 // two reductions (mean, then mean of squared deviations) and the output pass,
 // which keeps the kernel at 125 registers: two 256-thread CTAs per SM.
 // Shared memory holds the step's table rows: shift[C], then 1 + scale[C].
+// One row of modulate by one warp: LayerNorm statistics from the row held in
+// registers, then y = (x - mu) rstd * sc1 + sh with sc1 = 1 + scale (both
+// tables float32, read here from shared memory).
+template <int kChunks>
+__device__ __forceinline__ void modulate_row(const uint4 *__restrict__ x, void *__restrict__ y, int y_fp32,
+                                             int64_t row, int c, int lane, const float4 *sh4, const float4 *sc4,
+                                             float eps) {
+    const int cq = c >> 3;
+    const uint4 *xr = x + row * cq;
+    uint4 v[kChunks];
+#pragma unroll
+    for (int i = 0; i < kChunks; ++i) {
+        const int q = lane + 32 * i;
+        v[i] = q < cq ? __ldcs(xr + q) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kChunks; ++i) {
+        float f[8];
+        unpack8_fresh(v[i], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s += f[e];
+    }
+    const float mu = warp_sum(s) / (float)c;
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kChunks; ++i) {
+        if (lane + 32 * i < cq) {
+            float f[8];
+            unpack8_fresh(v[i], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float d = f[e] - mu;
+                ss = fmaf(d, d, ss);
+            }
+        }
+    }
+    const float rstd = 1.0f / sqrtf(warp_sum(ss) / (float)c + eps);
+#pragma unroll
+    for (int i = 0; i < kChunks; ++i) {
+        const int q = lane + 32 * i;
+        if (q < cq) {
+            float f[8];
+            unpack8_fresh(v[i], f);
+            const float4 a0 = sh4[2 * q], a1 = sh4[2 * q + 1];
+            const float4 b0 = sc4[2 * q], b1 = sc4[2 * q + 1];
+            const float sh[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float sc[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            float r[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) r[e] = fmaf((f[e] - mu) * rstd, sc[e], sh[e]);
+            if (y_fp32) {
+                float4 *yr = reinterpret_cast<float4 *>(y) + row * (int64_t)(2 * cq) + 2 * q;
+                __stcs(yr, make_float4(r[0], r[1], r[2], r[3]));
+                __stcs(yr + 1, make_float4(r[4], r[5], r[6], r[7]));
+            } else {
+                uint4 w;
+                w.x = pack_bf16x2(r[0], r[1]);
+                w.y = pack_bf16x2(r[2], r[3]);
+                w.z = pack_bf16x2(r[4], r[5]);
+                w.w = pack_bf16x2(r[6], r[7]);
+                __stcs(reinterpret_cast<uint4 *>(y) + row * cq + q, w);
+            }
+        }
+    }
+}
+
 template <int kChunks>
 __global__ void __launch_bounds__(kEwThreads, kChunks <= 21 ? 2 : 1)
     modulate_kernel(const uint4 *__restrict__ x, void *__restrict__ y, int y_fp32, int64_t n, int c,
@@ -68,68 +137,47 @@ __global__ void __launch_bounds__(kEwThreads, kChunks <= 21 ? 2 : 1)
     }
     __syncthreads();
     const int lane = (int)(threadIdx.x & 31);
-    const int cq = c >> 3;
     const float4 *sh4 = reinterpret_cast<const float4 *>(tab);
     const float4 *sc4 = reinterpret_cast<const float4 *>(tab + c);
     for (int64_t row = (int64_t)blockIdx.x * kEwWarps + (threadIdx.x >> 5); row < n;
-         row += (int64_t)gridDim.x * kEwWarps) {
-        const uint4 *xr = x + row * cq;
-        uint4 v[kChunks];
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-            const int q = lane + 32 * i;
-            v[i] = q < cq ? __ldcs(xr + q) : make_uint4(0u, 0u, 0u, 0u);
+         row += (int64_t)gridDim.x * kEwWarps)
+        modulate_row<kChunks>(x, y, y_fp32, row, c, lane, sh4, sc4, eps);
+}
+
+// Modulate with per-token modality rows, every modality's rows staged in
+// shared memory (num_tags x 2 x c floats, up to kTaggedSmemMax): one CTA of
+// 512 threads per SM, 16 rows in flight as in the untagged kernel.  A tag >=
+// num_tags skips the row and records kDevBadTag in the status word.
+constexpr int kTaggedThreads = 512;
+constexpr int kTaggedWarps = kTaggedThreads / 32;
+constexpr size_t kTaggedSmemMax = 200 * 1024;
+
+template <int kChunks>
+__global__ void __launch_bounds__(kTaggedThreads, 1)
+    modulate_tagged_smem_kernel(const uint4 *__restrict__ x, void *__restrict__ y, int y_fp32, int64_t n, int c,
+                                const float *__restrict__ shift_base, const float *__restrict__ scale_base,
+                                int64_t ld, int row_base, const uint8_t *__restrict__ tags, int num_tags, float eps,
+                                int *status) {
+    extern __shared__ float4 tab4[];
+    float *tab = reinterpret_cast<float *>(tab4);  // [num_tags][shift, 1 + scale][c]
+    for (int i = (int)threadIdx.x; i < num_tags * c; i += kTaggedThreads) {
+        const int t = i / c, j = i - t * c;
+        const int64_t src = (int64_t)(row_base + t) * ld + j;
+        tab[(2 * t) * c + j] = shift_base[src];
+        tab[(2 * t + 1) * c + j] = 1.0f + scale_base[src];
+    }
+    __syncthreads();
+    const int lane = (int)(threadIdx.x & 31);
+    for (int64_t row = (int64_t)blockIdx.x * kTaggedWarps + (threadIdx.x >> 5); row < n;
+         row += (int64_t)gridDim.x * kTaggedWarps) {
+        const int tag = (int)__ldg(tags + row);
+        if (tag >= num_tags) {
+            if (lane == 0) atomicCAS(status, 0, kDevBadTag);
+            continue;
         }
-        float s = 0.f;
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-            float f[8];
-            unpack8_fresh(v[i], f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) s += f[e];
-        }
-        const float mu = warp_sum(s) / (float)c;
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-            if (lane + 32 * i < cq) {
-                float f[8];
-                unpack8_fresh(v[i], f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float d = f[e] - mu;
-                    ss = fmaf(d, d, ss);
-                }
-            }
-        }
-        const float rstd = 1.0f / sqrtf(warp_sum(ss) / (float)c + eps);
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-            const int q = lane + 32 * i;
-            if (q < cq) {
-                float f[8];
-                unpack8_fresh(v[i], f);
-                const float4 a0 = sh4[2 * q], a1 = sh4[2 * q + 1];
-                const float4 b0 = sc4[2 * q], b1 = sc4[2 * q + 1];
-                const float sh[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float sc[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-                float r[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) r[e] = fmaf((f[e] - mu) * rstd, sc[e], sh[e]);
-                if (y_fp32) {
-                    float4 *yr = reinterpret_cast<float4 *>(y) + row * (int64_t)(2 * cq) + 2 * q;
-                    __stcs(yr, make_float4(r[0], r[1], r[2], r[3]));
-                    __stcs(yr + 1, make_float4(r[4], r[5], r[6], r[7]));
-                } else {
-                    uint4 w;
-                    w.x = pack_bf16x2(r[0], r[1]);
-                    w.y = pack_bf16x2(r[2], r[3]);
-                    w.z = pack_bf16x2(r[4], r[5]);
-                    w.w = pack_bf16x2(r[6], r[7]);
-                    __stcs(reinterpret_cast<uint4 *>(y) + row * cq + q, w);
-                }
-            }
-        }
+        const float4 *sh4 = reinterpret_cast<const float4 *>(tab + (size_t)(2 * tag) * c);
+        const float4 *sc4 = reinterpret_cast<const float4 *>(tab + (size_t)(2 * tag + 1) * c);
+        modulate_row<kChunks>(x, y, y_fp32, row, c, lane, sh4, sc4, eps);
     }
 }
 
@@ -175,9 +223,9 @@ __global__ void __launch_bounds__(kEwThreads) gated_residual_kernel(const uint4 
 }
 
 // Per-token modality rows: token i reads table row row_base + tags[i] (the
-// pages index the AdaLN table by timestep * 3 + token tag).  Table rows are
-// read through the read-only cache; a tag >= num_tags skips the row and
-// records kDevBadTag in the status word.
+// pages index the AdaLN table by timestep * 3 + token tag).  This version,
+// for tables too large to stage, reads the rows through the read-only cache;
+// a tag >= num_tags skips the row and records kDevBadTag in the status word.
 template <int kChunks>
 __global__ void __launch_bounds__(kEwThreads, kChunks <= 21 ? 2 : 1)
     modulate_tagged_kernel(const uint4 *__restrict__ x, void *__restrict__ y, int y_fp32, int64_t n, int c,
@@ -324,6 +372,32 @@ fv_status launch_modulate_t(const void *x, void *y, bool y_fp32, int64_t n, int 
 template <int kChunks>
 fv_status launch_modulate_tagged_t(const TaggedRows &t, const void *x, void *y, bool y_fp32, int64_t n, int c,
                                    float eps, int num_sms, cudaStream_t stream) {
+    // (rows wider than 21 chunks per lane would spill at 512 threads)
+    const size_t staged = (size_t)t.num_tags * 2 * (size_t)c * sizeof(float);
+    if constexpr (kChunks <= 21) {
+        if (staged <= kTaggedSmemMax) {
+            static std::mutex mu;
+            static bool attr_set[64] = {};
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FV_ERR_LAUNCH;
+            {
+                std::lock_guard<std::mutex> lk(mu);
+                if (!attr_set[dev]) {
+                    if (cudaFuncSetAttribute(modulate_tagged_smem_kernel<kChunks>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTaggedSmemMax) !=
+                        cudaSuccess)
+                        return FV_ERR_LAUNCH;
+                    attr_set[dev] = true;
+                }
+            }
+            const int64_t need = (n + kTaggedWarps - 1) / kTaggedWarps;
+            const int grid = (int)(need < num_sms ? need : num_sms);
+            modulate_tagged_smem_kernel<kChunks><<<grid, kTaggedThreads, staged, stream>>>(
+                static_cast<const uint4 *>(x), y, y_fp32 ? 1 : 0, n, c, t.table0, t.table1, t.ld, t.row_base, t.tags,
+                t.num_tags, eps, t.status);
+            return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
+        }
+    }
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, modulate_tagged_kernel<kChunks>, kEwThreads, 0) !=
             cudaSuccess ||
