@@ -206,7 +206,8 @@ def test_single_modality_tags_equal_untagged_call():
     y2 = fv.adaln_modulate(xm.cuda(), sh.cuda(), sc.cuda(), STEP, out_dtype=torch.float32)
     fv.sync_status()
     assert torch.equal(o1, o2)
-    assert float((y1 - y2).abs().max()) <= 1e-6
+    # the staged tagged modulate runs the untagged kernel's row code
+    assert torch.equal(y1, y2)
 
 
 def test_out_of_range_tag_is_reported_and_context_survives():
