@@ -53,14 +53,10 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// y = LN(x) * (1 + scale_row) + shift_row.  kChunks = 16-byte chunks per lane
-// per row (ceil(C / 256)); the packed bf16 row stays in registers between the
-// two reductions (mean, then mean of squared deviations) and the output pass,
-// which keeps the kernel at 125 registers: two 256-thread CTAs per SM.
-// Shared memory holds the step's table rows: shift[C], then 1 + scale[C].
 // One row of modulate by one warp: LayerNorm statistics from the row held in
 // registers, then y = (x - mu) rstd * sc1 + sh with sc1 = 1 + scale (both
-// tables float32, read here from shared memory).
+// tables float32, read here from shared memory).  kChunks = 16-byte chunks
+// per lane per row (ceil(C / 256)).
 template <int kChunks>
 __device__ __forceinline__ void modulate_row(const uint4 *__restrict__ x, void *__restrict__ y, int y_fp32,
                                              int64_t row, int c, int lane, const float4 *sh4, const float4 *sc4,
@@ -125,6 +121,11 @@ __device__ __forceinline__ void modulate_row(const uint4 *__restrict__ x, void *
     }
 }
 
+// y = LN(x) * (1 + scale_row) + shift_row.  kChunks = 16-byte chunks per lane
+// per row (ceil(C / 256)); the packed bf16 row stays in registers between the
+// two reductions (mean, then mean of squared deviations) and the output pass,
+// which keeps the kernel at 125 registers: two 256-thread CTAs per SM.
+// Shared memory holds the step's table rows: shift[C], then 1 + scale[C].
 template <int kChunks>
 __global__ void __launch_bounds__(kEwThreads, kChunks <= 21 ? 2 : 1)
     modulate_kernel(const uint4 *__restrict__ x, void *__restrict__ y, int y_fp32, int64_t n, int c,
