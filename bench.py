@@ -41,6 +41,17 @@ DATA = ("synthetic: seeded N(0,1) bf16 Q/K/V, residual x and branch output a; N(
         "(8 steps, step 3); no trained weights")
 
 
+# The pages' own figures, each on its own hardware and for its own scope:
+# context for the numbers above, not a target and not comparable with them.
+PAGES_CONTEXT = {
+    "attention_share_of_denoiser_runtime": {"value": ">85%", "kind": "reported", "model": "dense MiniMax H3"},
+    "seconds_per_sampling_step_72576_tokens": {
+        "values": {"32 GiB VRAM cap": 8.93, "8 GiB VRAM cap": 12.7, "8 GiB VRAM + 8 GiB RAM": 15.1},
+        "hardware": "1x H200 (capped)", "scope": "whole DiT step at 1344x768, 243 frames, weight streaming included"},
+    "end_to_end_10s_clip_1344x768_s": {"value": 122, "hardware": "GeForce RTX 5090 32 GB + 64 GB RAM",
+                                       "scope": "full two-pass pipeline (8 half- + 3 full-resolution steps)"},
+}
+
 def peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -573,6 +584,7 @@ def run_fv(args):
         "vdn_delta_attention": delta,
         "vsa_block_sparse_attention": vsa,
         "elementwise_alone": elementwise,
+        "context": PAGES_CONTEXT,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
