@@ -16,7 +16,7 @@ an 8 GB card", section "Where Video DeltaNet comes in":
 * two scans, forward and reverse, each seeded with S_T / 2 (the text state),
   so the two readouts together count it once.
 
-Readings where the page leaves the step open (listed in the design doc):
+Readings where the page leaves the step open:
 * the scans cover the frames the softmax branch does not treat as global
   anchors: forward over frames 1 .. F-2 and reverse over F-2 .. 1 (the first
   and last latent frames are softmax anchors);

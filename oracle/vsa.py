@@ -1,8 +1,8 @@
 """Oracle of VSA-style block-sparse attention over a video latent grid.
 
-TEST INFRASTRUCTURE ONLY (see the package docstring).  Plain numpy; the
-attention itself in float64, the tile selection in float32 (the precision the
-GPU path takes that integer decision in).
+TEST INFRASTRUCTURE ONLY (see the package docstring).  Plain numpy, float64
+throughout: the tile means, the coarse scores that decide the kept tiles, and
+the attention over them.
 
 What it computes, per head, following "FastH3 Preview v1: four calls,
 one-tenth the attention, and what the 14x actually measures", section
@@ -20,11 +20,15 @@ one-tenth the attention, and what the 14x actually measures", section
 * fine stage: every query of the tile attends exactly (softmax over
   scale * q.k) to the keys of its kept tiles, and to nothing else.
 
-Readings where the page leaves the step open (listed in the design doc):
+Readings where the page leaves the step open:
 * pooling is the plain mean over the tile's real tokens (an edge tile's mean
   is over its own, fewer, tokens); the coarse score is the dot product of the
   two means (the softmax scale and a row softmax do not change the ranking);
 * ties in the coarse score go to the lower tile index;
+* the page gives no precision for the coarse stage, so the oracle takes the
+  plain definition (means and dot products) in float64; a GPU path that
+  scores in float32 may keep a different tile only where two scores lie
+  within float32 rounding of each other;
 * the compression branch is left out: its gate is a trained projection that
   the base weights initialise to zero, so untrained it adds nothing;
 * only video tokens are present, so there are no exempt (always kept) keys
@@ -66,20 +70,20 @@ def tile_tokens(frames: int, height: int, width: int) -> list[np.ndarray]:
 
 
 def pooled(x: np.ndarray, tiles: list[np.ndarray]) -> np.ndarray:
-    """float32 mean of each tile's rows of x ([N, d] -> [num_tiles, d])."""
-    x32 = np.asarray(x, dtype=np.float32)
-    return np.stack([x32[idx].sum(axis=0, dtype=np.float32) / np.float32(len(idx)) for idx in tiles])
+    """float64 mean of each tile's rows of x ([N, d] -> [num_tiles, d])."""
+    x64 = np.asarray(x, dtype=np.float64)
+    return np.stack([x64[idx].sum(axis=0) / float(len(idx)) for idx in tiles])
 
 
 def coarse_scores(qbar: np.ndarray, kbar: np.ndarray) -> np.ndarray:
-    """float32 scores of every (query tile, key tile) pair."""
-    return (np.asarray(qbar, np.float32) @ np.asarray(kbar, np.float32).T).astype(np.float32)
+    """float64 scores of every (query tile, key tile) pair."""
+    return np.asarray(qbar, np.float64) @ np.asarray(kbar, np.float64).T
 
 
 def select(scores: np.ndarray, k: int) -> np.ndarray:
     """The k highest-scoring key tiles of each query tile, ties to the lower
     index; each row returned in ascending tile order ([num_tiles, k])."""
-    s = np.asarray(scores, dtype=np.float32).astype(np.float64)
+    s = np.asarray(scores, dtype=np.float64)
     index = np.broadcast_to(np.arange(s.shape[1]), s.shape)
     order = np.lexsort((index, -s), axis=-1)  # by descending score, then ascending index
     return np.sort(order[:, :k], axis=-1).astype(np.int64)

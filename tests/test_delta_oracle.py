@@ -122,6 +122,35 @@ def test_readout_uses_the_states_around_the_window():
     assert np.array_equal(fwd[frames - 1], fwd[frames - 2]) and np.array_equal(rev[0], rev[1])
 
 
+def test_readout_sees_only_frames_outside_the_window():
+    """The page: a frame reads a summary of the past before its softmax window
+    and of the future after it (the window itself is the softmax branch's).
+    With values zero everywhere except one written frame f, a query's readout
+    is non-zero exactly when f lies outside its window -- before it (carried
+    by the forward scan) or after it (by the reverse scan) -- and exactly zero
+    when f lies inside it.  The window is taken from its own definition: the
+    frames whose chunk is within window_chunks of the query's chunk."""
+    d, tok, frames, c, w = 8, 3, 16, 2, 1
+    n = tok * frames
+    rng = np.random.default_rng(21)
+    q, k = rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    beta = rng.uniform(0.5, 1.5, n)
+    alpha = np.ones((frames, d))
+    for f in range(1, frames - 1):  # the anchor frames 0 and F-1 are written by neither scan
+        v = np.zeros((n, d))
+        v[f * tok:(f + 1) * tok] = rng.standard_normal((tok, d))
+        rows = np.arange(n)
+        out, _, _ = V.delta_attn_head(q, k, v, beta, alpha, None, rows, tok, c, w)
+        for i in rows:
+            g = i // tok
+            inside = abs(f // c - g // c) <= w
+            mag = np.abs(out[i]).max()
+            if inside:
+                assert mag == 0.0, (f, g, mag)
+            else:
+                assert mag > 1e-6, (f, g, mag)
+
+
 def test_queries_and_keys_enter_only_through_their_directions():
     """The branch L2-normalises q and k: scaling a token's q or k changes nothing."""
     d, tok, frames = 6, 4, 7
@@ -147,6 +176,8 @@ MUTANTS = {
     "full_seed": ("0.5 * np.asarray(text_state, dtype=np.float64)", "np.asarray(text_state, dtype=np.float64)"),
     "window_off_by_one": ("p = max((c - window_chunks) * chunk_frames - 1, 0)", "p = max((c - window_chunks) * chunk_frames, 0)"),
     "no_key_normalisation": ("k_hat = l2_normalize(k)", "k_hat = k"),
+    "window_end_off_by_one": ("nx = min((c + window_chunks + 1) * chunk_frames, frames - 1)",
+                              "nx = min((c + window_chunks + 1) * chunk_frames - 1, frames - 1)"),
 }
 
 
@@ -175,6 +206,7 @@ def test_delta_mutant_is_caught(name, monkeypatch):
     checks = [test_update_is_the_argmin_autograd, test_update_matches_a_generic_minimiser,
               test_carried_state_never_grows, test_no_writes_pure_decay_and_seed_counted_once,
               test_strong_write_stores_the_value, test_readout_uses_the_states_around_the_window,
+              test_readout_sees_only_frames_outside_the_window,
               test_queries_and_keys_enter_only_through_their_directions]
     failed = 0
     for fn in checks:

@@ -56,7 +56,7 @@ def test_tile_means_are_over_the_tiles_own_tokens():
     assert np.array_equal(m, np.array([[b, -2.0 * b, 0.5] for b in range(len(tiles))], dtype=np.float32))
     y = np.random.default_rng(3).standard_normal((frames * height * width, 5)).astype(np.float32)
     mean = np.stack([[sum(float(y[i, c]) for i in idx) / len(idx) for c in range(5)] for idx in tiles])
-    assert np.abs(S.pooled(y, tiles) - mean).max() < 1e-6
+    assert np.abs(S.pooled(y, tiles) - mean).max() < 1e-12
 
 
 def test_selection_brute_force_with_ties():
@@ -69,6 +69,26 @@ def test_selection_brute_force_with_ties():
                     if sum(1 for o in range(11)
                            if scores[r, o] > scores[r, c] or (scores[r, o] == scores[r, c] and o < c)) < k]
             assert list(sel[r]) == want, (k, r)
+
+
+def test_selection_takes_the_exact_scores():
+    """The coarse scores are the plain dot products of the tile means: two key
+    tiles whose scores differ by 3e-8 (below float32 resolution at 1.0, where
+    they would tie and the lower index would win) are told apart."""
+    qbar = np.array([[1.0, 1.0]])
+    kbar = np.array([[1.0, 0.0], [1.0, 3e-8]])
+    sc = S.coarse_scores(qbar, kbar)
+    assert sc[0, 1] - sc[0, 0] == pytest.approx(3e-8, rel=1e-9)
+    assert list(S.select(sc, 1)[0]) == [1]
+    # means of the tiles' own rows feed the same decision
+    frames, height, width = 4, 4, 8  # two tiles side by side
+    tiles = S.tile_tokens(frames, height, width)
+    x = np.zeros((frames * height * width, 2))
+    for idx, row in zip(tiles, kbar):
+        x[idx] = row
+    kb = S.pooled(x, tiles)
+    assert np.abs(kb - kbar).max() <= 1e-20
+    assert list(S.select(S.coarse_scores(qbar, kb), 1)[0]) == [1]
 
 
 def test_zero_sparsity_is_dense_attention():
@@ -179,8 +199,11 @@ MUTANTS = {
     "no_minimum_of_one": ("max(1, min(int(", "max(0, min(int("),
     "grid_rounds_down": ("-(-width // TILE[2])", "(width // TILE[2])"),
     "height_width_swapped": ("(t * height + h) * width + w", "(t * width + w) * height + h"),
-    "mean_over_full_tile": ("/ np.float32(len(idx))", "/ np.float32(64)"),
+    "mean_over_full_tile": ("/ float(len(idx))", "/ 64.0"),
     "scale_dropped": ("s = scale * (k64[keys] @ q64[i])\n        e = np.exp", "s = (k64[keys] @ q64[i])\n        e = np.exp"),
+    "scores_in_float32": ("return np.asarray(qbar, np.float64) @ np.asarray(kbar, np.float64).T",
+                          "return (np.asarray(qbar, np.float32) @ np.asarray(kbar, np.float32).T)"
+                          ".astype(np.float64)"),
     "queries_pooled_from_keys": ("select(coarse_scores(pooled(q, tiles), pooled(k, tiles)), topk)",
                                  "select(coarse_scores(pooled(k, tiles), pooled(k, tiles)), topk)"),
     "row_tile_off_by_one": ("for c in selected[row_tile[i]]])\n        s = scale * (k64[keys] @ q64[i])\n        e =",
@@ -211,6 +234,7 @@ def test_vsa_mutant_is_caught(name, monkeypatch):
     monkeypatch.setattr(sys.modules[__name__], "S", _mutant_module(name))
     checks = [test_topk_count_follows_the_printed_formula, test_tile_grid_of_the_ten_second_clip,
               test_tile_means_are_over_the_tiles_own_tokens, test_selection_brute_force_with_ties,
+              test_selection_takes_the_exact_scores,
               test_zero_sparsity_is_dense_attention, test_one_kept_tile_by_hand, test_selection_follows_the_queries,
               test_values_of_dropped_tiles_do_not_matter, test_token_order_inside_a_tile_does_not_matter]
     failed = 0
