@@ -16,6 +16,7 @@
  *   fv_adaln_modulate_tagged, fv_gated_residual_tagged
  *                       the table row chosen per token (step and modality)
  *   fv_attn_fwd_noalloc fv_attn_fwd for callers that cannot allocate
+ *   fv_test_skip_load   test hook: make one bounded wait run out
  *
  * Sources ("FreeVideo: a 66 GB video transformer on an 8 GB card"):
  *   - section "What MiniMax H3 is, briefly": 56 heads of 128, Q/K/V 7168 wide,
@@ -331,6 +332,32 @@ fv_status fv_sync_status(void *stream);
 fv_status fv_attn_fwd_noalloc(const void *Q, const void *K, const void *V, void *O,
                               int64_t N, int H, int D, float scale, int head_group,
                               float *lse, void *stream, int *device_status_out);
+
+/*
+ * Test hook for the failure path; not for production use.  The pages have no
+ * counterpart.
+ *
+ * Every kernel that waits on a copy bounds that wait (about 2 s); a wait that
+ * runs out records FV_ERR_DEVICE_TIMEOUT in the status word, the kernel
+ * drains what it has in flight, releases its tensor memory and returns, and
+ * the context stays usable.  This call arms that path without any fault:
+ * the NEXT launch of the named kernel has its first CTA never issue the copy
+ * numbered load_index (counted from 0 in the order that CTA issues them:
+ * K/V tiles for FV_TEST_ATTN and FV_TEST_VSA_FINE, 64-token K/V stages for
+ * FV_TEST_VDA_STATS, inverse tiles M_t for FV_TEST_VDA_SCAN, Q tiles for
+ * FV_TEST_VDA_READOUT), so the wait for it runs out.  The hook is one-shot:
+ * that launch disarms it.  load_index < 0 disarms it without a launch.  A
+ * load_index the CTA never reaches leaves the launch unaffected.
+ * Returns FV_ERR_ARG for an unknown kernel.  Host only; thread-safe.
+ */
+typedef enum {
+    FV_TEST_ATTN = 0,         /* fv_attn_fwd, fv_attn_fwd_window, fv_attn_fwd_noalloc */
+    FV_TEST_VSA_FINE = 1,     /* the fine (block-sparse attention) kernel of fv_vsa_attn */
+    FV_TEST_VDA_STATS = 2,    /* the per-frame sums kernel of fv_delta_attn */
+    FV_TEST_VDA_SCAN = 3,     /* the state-scan kernel of fv_delta_attn */
+    FV_TEST_VDA_READOUT = 4   /* the readout kernel of fv_delta_attn */
+} fv_test_kernel;
+fv_status fv_test_skip_load(int kernel, int64_t load_index);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char *fv_status_string(fv_status s);

@@ -26,7 +26,7 @@ STATUS = {
 EXPORTS = ("fv_attn_fwd", "fv_adaln_modulate", "fv_gated_residual", "fv_step_for_timestep", "fv_sync_status",
            "fv_status_string", "fv_version", "fv_attn_fwd_noalloc", "fv_attn_fwd_window",
            "fv_adaln_modulate_tagged", "fv_gated_residual_tagged", "fv_delta_attn", "fv_vsa_attn",
-           "fv_vsa_num_tiles", "fv_vsa_topk", "fv_vsa_workspace_bytes")
+           "fv_vsa_num_tiles", "fv_vsa_topk", "fv_vsa_workspace_bytes", "fv_test_skip_load")
 NOALLOC_MAX_LAUNCHES = 64
 
 HEAD_DIM = 128
@@ -85,6 +85,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fv_version.restype = i32
     lib.fv_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, i64, i32, i32, f32, i32, vp, vp, ctypes.POINTER(ctypes.c_int)]
     lib.fv_attn_fwd_noalloc.restype = i32
+    lib.fv_test_skip_load.argtypes = [i32, i64]
+    lib.fv_test_skip_load.restype = i32
     if path is None:
         _lib = lib
     return lib
@@ -388,6 +390,18 @@ def step_for_timestep(ladder, t: float) -> int:
     _check(load_library().fv_step_for_timestep(arr, len(ladder), float(t), ctypes.byref(out)),
            "fv_step_for_timestep")
     return out.value
+
+
+# fv_test_kernel values (include/fv.h)
+TEST_ATTN, TEST_VSA_FINE, TEST_VDA_STATS, TEST_VDA_SCAN, TEST_VDA_READOUT = range(5)
+
+
+def test_skip_load(kernel: int, load_index: int) -> None:
+    """Test hook (fv_test_skip_load): the next launch of ``kernel`` has its
+    first CTA never issue copy number ``load_index``, so a bounded wait runs
+    out and the call reports FV_ERR_DEVICE_TIMEOUT.  One-shot; a negative
+    index disarms it."""
+    _check(load_library().fv_test_skip_load(int(kernel), int(load_index)), "fv_test_skip_load")
 
 
 def sync_status(stream=None) -> None:

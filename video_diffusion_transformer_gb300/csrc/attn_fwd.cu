@@ -36,7 +36,6 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
-#include <cstdlib>
 #include <mutex>
 
 #include "fv_internal.h"
@@ -94,7 +93,7 @@ struct Params {
     int kv_tiles;    // ceil(n / 128)
     int num_units;   // heads * q_blocks
     float scale_log2;  // scale * log2(e)
-    int skip_load;     // test hook: CTA 0 never issues its K/V load number skip_load (-1: off)
+    int64_t skip_load;  // test hook: CTA 0 never issues its K/V load number skip_load (-1: off)
     // windowed attention (0 frame tokens: dense): tokens form latent frames of
     // frame_tokens, frames form chunks of chunk_frames; a query sees the keys
     // of chunks within window_chunks of its own, plus the first and the last
@@ -737,11 +736,9 @@ fv_status launch_attn_fwd(const AttnLaunch &a, cudaStream_t stream) {
     p.kv_tiles = (int)((a.n + kRows - 1) / kRows);
     p.num_units = a.heads * p.q_blocks;
     p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
-    // Test hook for the failure path: FV_TEST_SKIP_KV_LOAD=<n> makes CTA 0 skip
-    // its n-th K/V tile load, so a bounded wait in the kernel runs out (about
-    // 2 s) and the call reports FV_ERR_DEVICE_TIMEOUT through fv_sync_status.
-    const char *skip = std::getenv("FV_TEST_SKIP_KV_LOAD");
-    p.skip_load = skip != nullptr ? std::atoi(skip) : -1;
+    // Test hook for the failure path (fv_test_skip_load, one-shot): CTA 0
+    // skips that K/V tile load, so a bounded wait in the kernel runs out.
+    p.skip_load = take_test_skip_load(FV_TEST_ATTN);
     p.frame_tokens = a.frame_tokens;
     p.chunk_frames = a.chunk_frames;
     p.window_chunks = a.window_chunks;

@@ -11,7 +11,6 @@
 // head-group launch -- in a fixed array compiled into the library.
 #include <cuda_runtime.h>
 
-#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -38,13 +37,6 @@ struct NoAllocDevice {
 std::mutex g_mu;
 NoAllocDevice g_devs[kMaxDevices];
 
-bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
-    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return x < y + nb && y < x + na;
-}
-
 // Once per device, with that device current: check the architecture, count
 // the SMs and look up the device address of the scratch array.  Nothing here
 // allocates.
@@ -54,13 +46,7 @@ fv_status setup_current_device(NoAllocDevice **out) {
     std::lock_guard<std::mutex> g(g_mu);
     NoAllocDevice &d = g_devs[dev];
     if (!d.ready) {
-        int major = 0, minor = 0, sms = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return FV_ERR_LAUNCH;
-        d.supported = (major == 10 && minor == 3);
-        d.num_sms = sms;
+        if (!fv::probe_device(dev, &d.supported, &d.num_sms)) return FV_ERR_LAUNCH;
         if (d.supported) {
             void *p = nullptr;
             if (cudaGetSymbolAddress(&p, g_noalloc_status) != cudaSuccess || p == nullptr) return FV_ERR_LAUNCH;
@@ -78,25 +64,13 @@ fv_status setup_current_device(NoAllocDevice **out) {
 extern "C" fv_status fv_attn_fwd_noalloc(const void *Q, const void *K, const void *V, void *O, int64_t N, int H,
                                          int D, float scale, int head_group, float *lse, void *stream,
                                          int *device_status_out) {
-    if (!Q || !K || !V || !O) return FV_ERR_NULL;
-    if (D != 128 || N < 1 || N >= (int64_t(1) << 31) || H < 1 || H > 256 || head_group < 1 || head_group > H)
-        return FV_ERR_SHAPE;
+    // the same checks as fv_attn_fwd, then the scratch limit
+    fv_status st = fv::check_attn_args(Q, K, V, O, N, H, D, scale, head_group, lse);
+    if (st != FV_OK) return st;
     const int launches = (H + head_group - 1) / head_group;
     if (launches > FV_NOALLOC_MAX_LAUNCHES) return FV_ERR_SHAPE;  // more launches than scratch words
-    if (!std::isfinite(scale) || scale < 0.0f) return FV_ERR_ARG;
-    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || (lse && !aligned(lse, 4)))
-        return FV_ERR_ALIGN;
-    const size_t bytes = (size_t)N * (size_t)H * 128u * 2u;
-    if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
-        return FV_ERR_ALIAS;
-    if (lse) {
-        const size_t lb = (size_t)N * (size_t)H * 4u;
-        if (overlaps(lse, lb, O, bytes) || overlaps(lse, lb, Q, bytes) || overlaps(lse, lb, K, bytes) ||
-            overlaps(lse, lb, V, bytes))
-            return FV_ERR_ALIAS;
-    }
     NoAllocDevice *d = nullptr;
-    fv_status st = setup_current_device(&d);
+    st = setup_current_device(&d);
     if (st != FV_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // The array keeps the previous call's words: clear the ones this call uses.

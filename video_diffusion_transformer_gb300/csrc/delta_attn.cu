@@ -153,6 +153,7 @@ fv_status launch_delta_attn(const DeltaLaunch &a, cudaStream_t stream) {
         const fv_status st = launch_vda_stats_tc(a, ws_m, ws_c, stream);
         if (st != FV_OK) return st;
         vda_solve_kernel<<<dim3(frames - 2, a.heads), kDThreads, 0, stream>>>(frames, ws_m);
+        if (cudaGetLastError() != cudaSuccess) return FV_ERR_LAUNCH;
     }
     const fv_status st = launch_vda_scan_tc(a, ws_m, ws_c, stream);
     if (st != FV_OK) return st;

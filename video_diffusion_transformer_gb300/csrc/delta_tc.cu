@@ -73,6 +73,7 @@ struct Params {
     int n, heads, frames, frame_tokens;
     int stages;         // stages per frame: ceil(frame_tokens / 64)
     int num_units;      // (frames - 2) * heads
+    int64_t skip_load;  // test hook: CTA 0 never issues its stage load number skip_load (-1: off)
 };
 
 struct Smem {
@@ -99,6 +100,9 @@ __device__ __forceinline__ void unit_of(const Params &p, int unit, int &frame, i
 
 __device__ void producer(const CUtensorMap *tk, const CUtensorMap *tv, const Params &p, const Smem &sm) {
     uint32_t g = 0;  // stages issued
+    // Test hook: a stage that is never loaded, so that the scalers' bounded
+    // wait runs out.  It must not be waited for in the drain below.
+    const int64_t skipped = blockIdx.x == 0 ? p.skip_load : -1;
     bool ok = true;
     for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
         int frame, head;
@@ -109,6 +113,7 @@ __device__ void producer(const CUtensorMap *tk, const CUtensorMap *tv, const Par
             if (!ok) break;
             const uint32_t base = sm.stages + slot * (uint32_t)kStageBytes;
             const int row = frame * p.frame_tokens + s * kTok;
+            if ((int64_t)g == skipped) continue;
             ptx::mbar_arrive_expect_tx(sm.b(kBarKvFull + (int)slot), 2 * kOperand);
             for (int c = 0; c < 2; ++c) {
                 ptx::tma_load_2d(base + kOffK + c * kHalf, tk, sm.b(kBarKvFull + (int)slot), head * kD + 64 * c, row);
@@ -119,7 +124,7 @@ __device__ void producer(const CUtensorMap *tk, const CUtensorMap *tv, const Par
     }
     for (uint32_t i = 0; i < (uint32_t)kStages && i < g; ++i) {
         const uint32_t last = g - 1u - i;
-        drain_bar(sm, kBarKvFull + (int)(last % kStages), (last / kStages) & 1u, p);
+        if ((int64_t)last != skipped) drain_bar(sm, kBarKvFull + (int)(last % kStages), (last / kStages) & 1u, p);
     }
 }
 
@@ -393,6 +398,7 @@ struct Params {
     __nv_bfloat16 *o;
     int *status;
     int n, ld, heads, chunk_tokens, chunks, tiles_per_chunk, tiles_per_part, num_items;
+    int64_t skip_load;  // test hook: CTA 0 never issues its Q tile load number skip_load (-1: off)
 };
 
 struct Smem {
@@ -436,6 +442,9 @@ __device__ __forceinline__ int tile_row0(const Params &p, const Item &it, int ti
 
 __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tw, const Params &p, const Smem &sm) {
     uint32_t g = 0, w = 0;  // Q tiles and W splits loaded
+    // Test hook: a Q tile that is never loaded, so that the MMA thread's
+    // bounded wait runs out.  It must not be waited for in the drain below.
+    const int64_t skipped = blockIdx.x == 0 ? p.skip_load : -1;
     bool ok = true;
     for (int i = blockIdx.x; ok && i < p.num_items; i += gridDim.x) {
         const Item it = item_of(p, i);
@@ -457,6 +466,7 @@ __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tw, const Par
             const uint32_t slot = g % kQStages;
             ok = wait_bar(sm, kBarEmpty + (int)slot, ((g / kQStages) & 1u) ^ 1u, p, kWhereEmpty);
             if (!ok) break;
+            if ((int64_t)g == skipped) continue;
             const uint32_t dst = sm.stages + kOffQ + slot * (uint32_t)kTile;
             const uint32_t bar = sm.b(kBarFull + (int)slot);
             ptx::mbar_arrive_expect_tx(bar, kTile);
@@ -467,7 +477,7 @@ __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tw, const Par
     // every copy issued must have landed before the CTA exits
     for (uint32_t k = 0; k < (uint32_t)kQStages && k < g; ++k) {
         const uint32_t last = g - 1u - k;
-        drain_bar(sm, kBarFull + (int)(last % kQStages), (last / kQStages) & 1u, p);
+        if ((int64_t)last != skipped) drain_bar(sm, kBarFull + (int)(last % kQStages), (last / kQStages) & 1u, p);
     }
     if (w > 0) drain_bar(sm, kBarWFull, (w - 1u) & 1u, p);
 }
@@ -709,6 +719,7 @@ struct Params {
     float *states;            // [2, heads, frames, 128, 128]
     int *status;
     int frames, heads;
+    int64_t skip_load;        // test hook: CTA (0, 0) never issues its M load number skip_load (-1: off)
 };
 
 struct Smem {
@@ -759,15 +770,19 @@ __device__ void control(const Params &p, const Smem &sm, uint32_t tmem, int h, i
     // B_k completes phase k - 1 of kBarB; the rows read it while forming U_k
     // (for k = 1 before the first step, else in the epilogue of step k - 1)
     uint32_t m_loads = 0, b_loads = 0;  // copies issued, for the drain
+    // Test hook: an M load that is never issued, so that this thread's
+    // bounded wait for it runs out.  It must not be waited for in the drain.
+    const int64_t skipped = (blockIdx.x == 0 && blockIdx.y == 0) ? p.skip_load : -1;
+    auto load_m = [&](uint32_t dst, int step, uint32_t bar) {
+        if ((int64_t)m_loads != skipped) load64k(dst, mtile(step), bar);
+        ++m_loads;
+    };
     if (steps >= 1) {
-        load64k(sm.m, mtile(1), sm.b(kBarM));
+        load_m(sm.m, 1, sm.b(kBarM));
         load_b(1);
-        m_loads = b_loads = 1;
+        b_loads = 1;
     }
-    if (steps >= 2) {
-        load64k(sm.m + (uint32_t)kMBytes, mtile(2), sm.b(kBarM + 1));
-        m_loads = 2;
-    }
+    if (steps >= 2) load_m(sm.m + (uint32_t)kMBytes, 2, sm.b(kBarM + 1));
     constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, true);
     const uint32_t t_d = tmem, t_hi = tmem + 128u, t_lo = tmem + 192u;
     bool ok = wait_bar(sm, kBarA, 0u, p, kWhereA);  // U_1 split in tensor memory, B_1 read
@@ -796,10 +811,7 @@ __device__ void control(const Params &p, const Smem &sm, uint32_t tmem, int h, i
         // the MMAs have read this M buffer: refill it two steps ahead
         ok = wait_bar(sm, kBarD, (uint32_t)((s - 1) & 1), p, kWhereD);
         if (!ok) break;
-        if (s + 2 <= steps) {
-            load64k(sm.m + (uint32_t)(buf * kMBytes), mtile(s + 2), sm.b(kBarM + buf));
-            ++m_loads;
-        }
+        if (s + 2 <= steps) load_m(sm.m + (uint32_t)(buf * kMBytes), s + 2, sm.b(kBarM + buf));
         // the rows have stored S_s, read B_{s+1} and written U_{s+1}'s split
         ok = wait_bar(sm, kBarA, (uint32_t)(s & 1), p, kWhereA);
         if (!ok) break;
@@ -812,7 +824,8 @@ __device__ void control(const Params &p, const Smem &sm, uint32_t tmem, int h, i
     // every copy issued must have landed before the CTA exits
     int never = 0;
     for (uint32_t i = m_loads > 2u ? m_loads - 2u : 0u; i < m_loads; ++i)
-        ptx::mbar_wait(sm.b(kBarM + (int)(i & 1u)), (i >> 1) & 1u, &never, p.status, kDevTimeout | kWhereDrain);
+        if ((int64_t)i != skipped)
+            ptx::mbar_wait(sm.b(kBarM + (int)(i & 1u)), (i >> 1) & 1u, &never, p.status, kDevTimeout | kWhereDrain);
     if (b_loads > 0)
         ptx::mbar_wait(sm.b(kBarB), (b_loads - 1u) & 1u, &never, p.status, kDevTimeout | kWhereDrain);
 }
@@ -1040,6 +1053,7 @@ fv_status launch_vda_stats_tc(const DeltaLaunch &a, float *ws_m, float *ws_c, cu
     p.frame_tokens = a.frame_tokens;
     p.stages = (a.frame_tokens + kTok - 1) / kTok;
     p.num_units = (frames - 2) * a.heads;
+    p.skip_load = take_test_skip_load(FV_TEST_VDA_STATS);
     const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
     vda_stats_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
@@ -1068,6 +1082,7 @@ fv_status launch_vda_scan_tc(const DeltaLaunch &a, const float *ws_m, const floa
     p.status = a.status;
     p.frames = (int)(a.n / a.frame_tokens);
     p.heads = a.heads;
+    p.skip_load = take_test_skip_load(FV_TEST_VDA_SCAN);
     vda_scan_tc_kernel<<<dim3(a.heads, 2), sc::kThreads, sc::kSmemBytes, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
 }
@@ -1108,6 +1123,7 @@ fv_status launch_vda_readout_tc(const DeltaLaunch &a, __nv_bfloat16 *wsplit, cud
     // every chunk but the last holds chunk_tokens rows; the last one's extra
     // tiles (past the sequence) are still dealt out and store nothing
     p.num_items = chunks * a.heads * ro::kParts;
+    p.skip_load = take_test_skip_load(FV_TEST_VDA_READOUT);
     const int grid = p.num_items < a.num_sms ? p.num_items : a.num_sms;
     vda_readout_tc_kernel<<<grid, ro::kThreads, ro::kSmemBytes, stream>>>(mq, mw, p);
     return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;

@@ -53,14 +53,40 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Where modulate_row reads a row's table values: shift and 1 + scale for the
+// 8 channels of chunk q.  Staged: both already in shared memory (1 + scale
+// precomputed).  Cached: both rows in global memory, read through the
+// read-only cache, 1 is added here (the same float32 sum as when staging).
+struct StagedRows {
+    const float4 *sh4, *sc4;
+    __device__ __forceinline__ void get(int q, float (&sh)[8], float (&sc1)[8]) const {
+        const float4 a0 = sh4[2 * q], a1 = sh4[2 * q + 1];
+        const float4 b0 = sc4[2 * q], b1 = sc4[2 * q + 1];
+        sh[0] = a0.x; sh[1] = a0.y; sh[2] = a0.z; sh[3] = a0.w; sh[4] = a1.x; sh[5] = a1.y; sh[6] = a1.z; sh[7] = a1.w;
+        sc1[0] = b0.x; sc1[1] = b0.y; sc1[2] = b0.z; sc1[3] = b0.w;
+        sc1[4] = b1.x; sc1[5] = b1.y; sc1[6] = b1.z; sc1[7] = b1.w;
+    }
+};
+
+struct CachedRows {
+    const float4 *sh4, *sc4;
+    __device__ __forceinline__ void get(int q, float (&sh)[8], float (&sc1)[8]) const {
+        const float4 a0 = __ldg(sh4 + 2 * q), a1 = __ldg(sh4 + 2 * q + 1);
+        const float4 b0 = __ldg(sc4 + 2 * q), b1 = __ldg(sc4 + 2 * q + 1);
+        sh[0] = a0.x; sh[1] = a0.y; sh[2] = a0.z; sh[3] = a0.w; sh[4] = a1.x; sh[5] = a1.y; sh[6] = a1.z; sh[7] = a1.w;
+        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sc1[e] = 1.0f + b[e];
+    }
+};
+
 // One row of modulate by one warp: LayerNorm statistics from the row held in
 // registers, then y = (x - mu) rstd * sc1 + sh with sc1 = 1 + scale (both
-// tables float32, read here from shared memory).  kChunks = 16-byte chunks
-// per lane per row (ceil(C / 256)).
-template <int kChunks>
+// float32, from `rows`).  kChunks = 16-byte chunks per lane per row
+// (ceil(C / 256)).
+template <int kChunks, class Rows>
 __device__ __forceinline__ void modulate_row(const uint4 *__restrict__ x, void *__restrict__ y, int y_fp32,
-                                             int64_t row, int c, int lane, const float4 *sh4, const float4 *sc4,
-                                             float eps) {
+                                             int64_t row, int c, int lane, const Rows &rows, float eps) {
     const int cq = c >> 3;
     const uint4 *xr = x + row * cq;
     uint4 v[kChunks];
@@ -98,10 +124,8 @@ __device__ __forceinline__ void modulate_row(const uint4 *__restrict__ x, void *
         if (q < cq) {
             float f[8];
             unpack8_fresh(v[i], f);
-            const float4 a0 = sh4[2 * q], a1 = sh4[2 * q + 1];
-            const float4 b0 = sc4[2 * q], b1 = sc4[2 * q + 1];
-            const float sh[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float sc[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            float sh[8], sc[8];
+            rows.get(q, sh, sc);
             float r[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) r[e] = fmaf((f[e] - mu) * rstd, sc[e], sh[e]);
@@ -138,11 +162,10 @@ __global__ void __launch_bounds__(kEwThreads, kChunks <= 21 ? 2 : 1)
     }
     __syncthreads();
     const int lane = (int)(threadIdx.x & 31);
-    const float4 *sh4 = reinterpret_cast<const float4 *>(tab);
-    const float4 *sc4 = reinterpret_cast<const float4 *>(tab + c);
+    const StagedRows rows{reinterpret_cast<const float4 *>(tab), reinterpret_cast<const float4 *>(tab + c)};
     for (int64_t row = (int64_t)blockIdx.x * kEwWarps + (threadIdx.x >> 5); row < n;
          row += (int64_t)gridDim.x * kEwWarps)
-        modulate_row<kChunks>(x, y, y_fp32, row, c, lane, sh4, sc4, eps);
+        modulate_row<kChunks>(x, y, y_fp32, row, c, lane, rows, eps);
 }
 
 // Modulate with per-token modality rows, every modality's rows staged in
@@ -176,9 +199,9 @@ __global__ void __launch_bounds__(kTaggedThreads, 1)
             if (lane == 0) atomicCAS(status, 0, kDevBadTag);
             continue;
         }
-        const float4 *sh4 = reinterpret_cast<const float4 *>(tab + (size_t)(2 * tag) * c);
-        const float4 *sc4 = reinterpret_cast<const float4 *>(tab + (size_t)(2 * tag + 1) * c);
-        modulate_row<kChunks>(x, y, y_fp32, row, c, lane, sh4, sc4, eps);
+        const StagedRows rows{reinterpret_cast<const float4 *>(tab + (size_t)(2 * tag) * c),
+                              reinterpret_cast<const float4 *>(tab + (size_t)(2 * tag + 1) * c)};
+        modulate_row<kChunks>(x, y, y_fp32, row, c, lane, rows, eps);
     }
 }
 
@@ -233,7 +256,6 @@ __global__ void __launch_bounds__(kEwThreads, kChunks <= 21 ? 2 : 1)
                            const float *__restrict__ shift_base, const float *__restrict__ scale_base, int64_t ld,
                            int row_base, const uint8_t *__restrict__ tags, int num_tags, float eps, int *status) {
     const int lane = (int)(threadIdx.x & 31);
-    const int cq = c >> 3;
     for (int64_t row = (int64_t)blockIdx.x * kEwWarps + (threadIdx.x >> 5); row < n;
          row += (int64_t)gridDim.x * kEwWarps) {
         const int tag = (int)__ldg(tags + row);
@@ -241,65 +263,9 @@ __global__ void __launch_bounds__(kEwThreads, kChunks <= 21 ? 2 : 1)
             if (lane == 0) atomicCAS(status, 0, kDevBadTag);
             continue;
         }
-        const float4 *sh4 = reinterpret_cast<const float4 *>(shift_base + (int64_t)(row_base + tag) * ld);
-        const float4 *sc4 = reinterpret_cast<const float4 *>(scale_base + (int64_t)(row_base + tag) * ld);
-        const uint4 *xr = x + row * cq;
-        uint4 v[kChunks];
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-            const int q = lane + 32 * i;
-            v[i] = q < cq ? __ldcs(xr + q) : make_uint4(0u, 0u, 0u, 0u);
-        }
-        float s = 0.f;
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-            float f[8];
-            unpack8_fresh(v[i], f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) s += f[e];
-        }
-        const float mu = warp_sum(s) / (float)c;
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-            if (lane + 32 * i < cq) {
-                float f[8];
-                unpack8_fresh(v[i], f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float d = f[e] - mu;
-                    ss = fmaf(d, d, ss);
-                }
-            }
-        }
-        const float rstd = 1.0f / sqrtf(warp_sum(ss) / (float)c + eps);
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-            const int q = lane + 32 * i;
-            if (q < cq) {
-                float f[8];
-                unpack8_fresh(v[i], f);
-                const float4 a0 = __ldg(sh4 + 2 * q), a1 = __ldg(sh4 + 2 * q + 1);
-                const float4 b0 = __ldg(sc4 + 2 * q), b1 = __ldg(sc4 + 2 * q + 1);
-                const float sh[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float sc[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-                float r[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) r[e] = fmaf((f[e] - mu) * rstd, 1.0f + sc[e], sh[e]);
-                if (y_fp32) {
-                    float4 *yr = reinterpret_cast<float4 *>(y) + row * (int64_t)(2 * cq) + 2 * q;
-                    __stcs(yr, make_float4(r[0], r[1], r[2], r[3]));
-                    __stcs(yr + 1, make_float4(r[4], r[5], r[6], r[7]));
-                } else {
-                    uint4 w;
-                    w.x = pack_bf16x2(r[0], r[1]);
-                    w.y = pack_bf16x2(r[2], r[3]);
-                    w.z = pack_bf16x2(r[4], r[5]);
-                    w.w = pack_bf16x2(r[6], r[7]);
-                    __stcs(reinterpret_cast<uint4 *>(y) + row * cq + q, w);
-                }
-            }
-        }
+        const CachedRows rows{reinterpret_cast<const float4 *>(shift_base + (int64_t)(row_base + tag) * ld),
+                              reinterpret_cast<const float4 *>(scale_base + (int64_t)(row_base + tag) * ld)};
+        modulate_row<kChunks>(x, y, y_fp32, row, c, lane, rows, eps);
     }
 }
 

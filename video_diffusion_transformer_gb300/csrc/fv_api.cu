@@ -2,6 +2,7 @@
 // host, device checks, the per-device status word, and head-group launches.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -23,6 +24,10 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
+// fv_test_skip_load's armed load index per fv_test_kernel (-1: disarmed).
+constexpr int kTestKernels = 5;
+std::atomic<int64_t> g_test_skip[kTestKernels] = {{-1}, {-1}, {-1}, {-1}, {-1}};
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
@@ -38,13 +43,7 @@ fv_status device_state(DeviceState **out) {
     std::lock_guard<std::mutex> g(g_mu);
     DeviceState &d = g_dev[dev];
     if (!d.probed) {
-        int major = 0, minor = 0, sms = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return FV_ERR_LAUNCH;
-        d.supported = (major == 10 && minor == 3);
-        d.num_sms = sms;
+        if (!fv::probe_device(dev, &d.supported, &d.num_sms)) return FV_ERR_LAUNCH;
         d.probed = true;
     }
     if (!d.supported) return FV_ERR_UNSUPPORTED_DEVICE;
@@ -66,23 +65,10 @@ fv_status device_state(DeviceState **out) {
 fv_status attn_common(const void *Q, const void *K, const void *V, void *O, int64_t N, int H, int D, float scale,
                       int head_group, int frame_tokens, int chunk_frames, int window_chunks, float *lse,
                       void *stream) {
-    if (!Q || !K || !V || !O) return FV_ERR_NULL;
-    if (D != 128 || N < 1 || N >= (int64_t(1) << 31) || H < 1 || H > 256 || head_group < 1 || head_group > H)
-        return FV_ERR_SHAPE;
-    if (!std::isfinite(scale) || scale < 0.0f) return FV_ERR_ARG;
-    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || (lse && !aligned(lse, 4)))
-        return FV_ERR_ALIGN;
-    const size_t bytes = (size_t)N * (size_t)H * 128u * 2u;
-    if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
-        return FV_ERR_ALIAS;
-    if (lse) {
-        const size_t lb = (size_t)N * (size_t)H * 4u;
-        if (overlaps(lse, lb, O, bytes) || overlaps(lse, lb, Q, bytes) || overlaps(lse, lb, K, bytes) ||
-            overlaps(lse, lb, V, bytes))
-            return FV_ERR_ALIAS;
-    }
+    fv_status st = fv::check_attn_args(Q, K, V, O, N, H, D, scale, head_group, lse);
+    if (st != FV_OK) return st;
     DeviceState *d = nullptr;
-    fv_status st = device_state(&d);
+    st = device_state(&d);
     if (st != FV_OK) return st;
     fv::AttnLaunch a;
     a.q = Q;
@@ -108,6 +94,46 @@ fv_status attn_common(const void *Q, const void *K, const void *V, void *O, int6
 }
 
 }  // namespace
+
+namespace fv {
+bool probe_device(int dev, bool *supported, int *num_sms) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    *supported = (major == 10 && minor == 3);
+    *num_sms = sms;
+    return true;
+}
+
+fv_status check_attn_args(const void *Q, const void *K, const void *V, const void *O, int64_t N, int H, int D,
+                          float scale, int head_group, const float *lse) {
+    if (!Q || !K || !V || !O) return FV_ERR_NULL;
+    if (D != 128 || N < 1 || N >= (int64_t(1) << 31) || H < 1 || H > 256 || head_group < 1 || head_group > H)
+        return FV_ERR_SHAPE;
+    if (!std::isfinite(scale) || scale < 0.0f) return FV_ERR_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || (lse && !aligned(lse, 4)))
+        return FV_ERR_ALIGN;
+    const size_t bytes = (size_t)N * (size_t)H * 128u * 2u;
+    if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
+        return FV_ERR_ALIAS;
+    if (lse) {
+        const size_t lb = (size_t)N * (size_t)H * 4u;
+        if (overlaps(lse, lb, O, bytes) || overlaps(lse, lb, Q, bytes) || overlaps(lse, lb, K, bytes) ||
+            overlaps(lse, lb, V, bytes))
+            return FV_ERR_ALIAS;
+    }
+    return FV_OK;
+}
+
+int64_t take_test_skip_load(int kernel) {
+    if (kernel < 0 || kernel >= kTestKernels) return -1;
+    // a plain load first: launches with the hook disarmed never write the atomic
+    if (g_test_skip[kernel].load(std::memory_order_relaxed) < 0) return -1;
+    return g_test_skip[kernel].exchange(-1);
+}
+}  // namespace fv
 
 extern "C" {
 
@@ -358,6 +384,12 @@ const char *fv_status_string(fv_status s) {
     return "unknown fv_status";
 }
 
-int fv_version(void) { return 100; }
+fv_status fv_test_skip_load(int kernel, int64_t load_index) {
+    if (kernel < 0 || kernel >= kTestKernels) return FV_ERR_ARG;
+    g_test_skip[kernel].store(load_index < 0 ? -1 : load_index);
+    return FV_OK;
+}
+
+int fv_version(void) { return 200; }
 
 }  // extern "C"

@@ -16,6 +16,20 @@ constexpr int kDevTimeout = 0x7100;
 // A per-token modality tag was >= the number of modalities; the row was skipped.
 constexpr int kDevBadTag = 0x7200;
 
+// Compute capability check (10.3) and SM count of device `dev`; false if a
+// runtime query fails.
+bool probe_device(int dev, bool *supported, int *num_sms);
+
+// The host-side argument checks every attention entry point makes (pointers,
+// sizes, scale, 16-byte alignment, forbidden overlaps); FV_OK or the status
+// the call returns without enqueueing anything.
+fv_status check_attn_args(const void *Q, const void *K, const void *V, const void *O, int64_t N, int H, int D,
+                          float scale, int head_group, const float *lse);
+
+// The load index armed by fv_test_skip_load for `kernel` (an fv_test_kernel
+// value), or -1; reading it disarms the hook.
+int64_t take_test_skip_load(int kernel);
+
 // cuTensorMapEncodeTiled, looked up once through the runtime (null if absent).
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,

@@ -363,6 +363,7 @@ struct Params {
     Geo g;
     int n, ld, pairs, num_units, list_ld;
     float scale_log2;
+    int64_t skip_load;      // test hook: CTA 0 never issues its K/V load number skip_load (-1: off)
 };
 
 struct Smem {
@@ -472,6 +473,9 @@ struct MaskWindow {
 __device__ void producer(const CUtensorMap *tq, const Params &p, const Smem &sm, int lane) {
     if (lane != 0) return;
     uint32_t loads = 0, q_loads = 0;
+    // Test hook: a load that is never issued, so that a consumer's bounded
+    // wait runs out.  It must not be waited for in the drain below.
+    const int64_t skipped = blockIdx.x == 0 ? p.skip_load : -1;
     bool ok = true;
     for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
         const int head = unit / p.pairs, pr = unit % p.pairs;
@@ -492,10 +496,12 @@ __device__ void producer(const CUtensorMap *tq, const Params &p, const Smem &sm,
             if (!wait_bar(sm, kBarKvEmpty + (int)s, ph ^ 1u, p, kWhereKvEmpty)) return false;
             const int e0 = 2 * j < cnt ? lst[2 * j] : 0xFFFF, e1 = 2 * j + 1 < cnt ? lst[2 * j + 1] : 0xFFFF;
             const uint32_t full = sm.b(kBarKvFull + (int)(loads % kKvFullBars));
-            ptx::mbar_arrive_expect_tx(full, kTileBytes);
-            const uint32_t dst = sm.kv + s * (uint32_t)kTileBytes;
-            load_kv_tile(m, p, dst, 0, head, e0 & 0xFFFF, full);
-            load_kv_tile(m, p, dst, 1, head, e1 & 0xFFFF, full);
+            if ((int64_t)loads != skipped) {
+                ptx::mbar_arrive_expect_tx(full, kTileBytes);
+                const uint32_t dst = sm.kv + s * (uint32_t)kTileBytes;
+                load_kv_tile(m, p, dst, 0, head, e0 & 0xFFFF, full);
+                load_kv_tile(m, p, dst, 1, head, e1 & 0xFFFF, full);
+            }
             ++loads;
             return true;
         };
@@ -508,7 +514,7 @@ __device__ void producer(const CUtensorMap *tq, const Params &p, const Smem &sm,
     }
     // the last kKvFullBars loads each hold their own full barrier
     for (uint32_t l = loads > (uint32_t)kKvFullBars ? loads - kKvFullBars : 0u; l < loads; ++l)
-        drain_bar(sm, kBarKvFull + (int)(l % kKvFullBars), (l / kKvFullBars) & 1u, p);
+        if ((int64_t)l != skipped) drain_bar(sm, kBarKvFull + (int)(l % kKvFullBars), (l / kKvFullBars) & 1u, p);
     for (uint32_t i = 0; i < (uint32_t)kQSlots && i < q_loads; ++i) {
         const uint32_t last = q_loads - 1u - i;
         drain_bar(sm, kBarQFull + (int)(last % kQSlots), (last / kQSlots) & 1u, p);
@@ -1029,6 +1035,7 @@ fv_status launch_vsa_attn(const VsaLaunch &a, cudaStream_t stream) {
     p.num_units = a.heads * pairs;
     p.list_ld = 2 * a.topk;
     p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
+    p.skip_load = take_test_skip_load(FV_TEST_VSA_FINE);
     const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
     vsa_fine_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, p);
     return cudaGetLastError() == cudaSuccess ? FV_OK : FV_ERR_LAUNCH;
