@@ -68,7 +68,8 @@ typedef enum {
     FV_ERR_LAUNCH = -6,              /* a CUDA call or kernel launch failed */
     FV_ERR_DEVICE_TIMEOUT = -7,      /* a bounded wait inside a kernel ran out */
     FV_ERR_ARG = -8,                 /* a scalar argument is invalid (scale < 0, eps < 0, NaN, ...) */
-    FV_ERR_ALIAS = -9                /* buffers overlap where the call forbids it */
+    FV_ERR_ALIAS = -9,               /* buffers overlap where the call forbids it */
+    FV_ERR_DEVICE_CHECK = -10        /* debug build only: an in-kernel index check failed */
 } fv_status;
 
 /*
@@ -295,7 +296,15 @@ fv_status fv_step_for_timestep(const float *ladder, int num_steps, float t, int 
  * Synchronise `stream`, then read and clear the current device's status word.
  * Returns FV_OK, FV_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait
  * since the last call, FV_ERR_ARG if a kernel met an out-of-range token tag,
+ * FV_ERR_DEVICE_CHECK if (debug build only) an in-kernel index check failed,
  * or FV_ERR_LAUNCH if the stream reports a CUDA error.
+ *
+ * Debug build: the library compiled with FV_DEBUG_CHECKS=1 (libfv_debug.so,
+ * made next to libfv.so by the package's build step) checks, inside the
+ * attention kernels, every tile coordinate against N and the head range
+ * and every tensor-memory column against the allocation before it is used;
+ * a failed check records FV_ERR_DEVICE_CHECK here and skips the access
+ * instead of trapping.  The release build compiles the checks out.
  */
 fv_status fv_sync_status(void *stream);
 
@@ -326,7 +335,8 @@ fv_status fv_sync_status(void *stream);
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
  * device_status_out: NULL to return right after enqueueing (device-side
  *   timeouts then go unreported); otherwise the call synchronises `stream`,
- *   then writes FV_OK or FV_ERR_DEVICE_TIMEOUT to *device_status_out.
+ *   then writes FV_OK or FV_ERR_DEVICE_TIMEOUT (FV_ERR_DEVICE_CHECK from a
+ *   failed index check of the debug build) to *device_status_out.
  */
 #define FV_NOALLOC_MAX_LAUNCHES 64
 fv_status fv_attn_fwd_noalloc(const void *Q, const void *K, const void *V, void *O,

@@ -16,11 +16,13 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libfv.so")
+# the same library with the in-kernel index checks compiled in (FV_DEBUG_CHECKS=1)
+DEBUG_LIB_PATH = os.path.join(_HERE, "_build", "libfv_debug.so")
 
 STATUS = {
     0: "FV_OK", -1: "FV_ERR_NULL", -2: "FV_ERR_SHAPE", -3: "FV_ERR_ALIGN", -4: "FV_ERR_STEP",
     -5: "FV_ERR_UNSUPPORTED_DEVICE", -6: "FV_ERR_LAUNCH", -7: "FV_ERR_DEVICE_TIMEOUT", -8: "FV_ERR_ARG",
-    -9: "FV_ERR_ALIAS",
+    -9: "FV_ERR_ALIAS", -10: "FV_ERR_DEVICE_CHECK",
 }
 # every symbol include/fv.h declares
 EXPORTS = ("fv_attn_fwd", "fv_adaln_modulate", "fv_gated_residual", "fv_step_for_timestep", "fv_sync_status",

@@ -81,6 +81,9 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 // where codes for the status word
 constexpr int kWhereQEmpty = 1, kWhereKvEmpty = 2, kWhereQFull = 3, kWhereKvFull = 4, kWherePFull = 5,
               kWhereSFull = 6, kWhereOFull = 7, kWhereDrain = 8;
+// index checks of the debug build (dev_check): Q tile, K/V tile, tensor
+// memory columns, output row store, LSE store
+constexpr int kChkQTile = 0x11, kChkKvTile = 0x12, kChkTmem = 0x13, kChkStore = 0x14, kChkLse = 0x15;
 
 struct Params {
     __nv_bfloat16 *o;
@@ -239,7 +242,10 @@ __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUt
         ok = wait_bar(sm, kBarQEmpty, (q_loads & 1u) ^ 1u, p, kWhereQEmpty);
         if (!ok) break;
         ptx::mbar_arrive_expect_tx(sm.b(kBarQFull), kQTiles * kTileBytes);
-        for (int k = 0; k < kQTiles; ++k) {
+        const bool q_ok = dev_check(qb >= 0 && qb < p.q_blocks && head_off >= 0 &&
+                                        head_off < p.num_units / p.q_blocks && x0 + kD <= p.ld,
+                                    p.status, kChkQTile);
+        for (int k = 0; q_ok && k < kQTiles; ++k) {
             const int y = qb * kUnitRows + k * kRows;
             const uint32_t dst = sm.q + (uint32_t)(k * kTileBytes);
             ptx::tma_load_2d(dst, tq, sm.b(kBarQFull), x0, y);
@@ -249,11 +255,14 @@ __device__ void producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUt
         const KvList kl = kv_list<kWindow>(p, qb);
         for (int j = 0; ok && j < kl.count; ++j) {
             const int kv_row = kl.tile(j) * kRows;
+            // tiles inside the sequence, ascending (every role derives the same list)
+            const bool kv_ok = dev_check(kv_row >= 0 && kv_row < p.n && (j == 0 || kl.tile(j) > kl.tile(j - 1)),
+                                         p.status, kChkKvTile);
             for (int w = 0; w < 2; ++w) {
                 const uint32_t s = loads % kStages, ph = (loads / kStages) & 1u;
                 ok = wait_bar(sm, kBarKvEmpty + (int)s, ph ^ 1u, p, kWhereKvEmpty);
                 if (!ok) break;
-                if ((int64_t)loads != skipped) {
+                if ((int64_t)loads != skipped && kv_ok) {
                     ptx::mbar_arrive_expect_tx(sm.b(kBarKvFull + (int)s), kTileBytes);
                     const CUtensorMap *m = w ? tv : tk;
                     const uint32_t dst = sm.kv + s * (uint32_t)kTileBytes;
@@ -309,6 +318,9 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 
 template <bool kWindow>
 __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
+    // S_k and P_k at columns [128 k, 128 k + 128), O_k at [256 + 128 k, 384 + 128 k)
+    if (!dev_check(256u + 128u * (kQTiles - 1) + 128u <= kTmemCols && 128u * kQTiles <= 256u, p.status, kChkTmem))
+        return;
     MmaDescs dsc;
     dsc.q0 = ptx::sdesc_sw128(sm.q, 16, 1024);
     dsc.kv0 = ptx::sdesc_sw128(sm.kv, 16, 1024);
@@ -489,6 +501,7 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
             if (!ok) break;
             ptx::tc_fence_after();
             const int kb = (kWindow ? kl.tile(j) : j) * kRows;
+            dev_check(kb >= 0 && kb < p.n && (t >> 5) < 4, p.status, kChkKvTile);
             ColMask<kWindow> cm;
             cm.valid = p.n - kb;
             cm.all = !kWindow || rw.anchor;
@@ -585,7 +598,7 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
         if (!ok) break;
         ptx::tc_fence_after();
         const float inv_l = 1.0f / l;
-        const bool row_ok = row < p.n;
+        const bool row_ok = row < p.n && dev_check(head * kD + kD <= p.ld, p.status, kChkStore);
         uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(row_ok ? row : 0) * (size_t)p.ld + (size_t)head * kD);
 #pragma unroll 1
         for (int c4 = 0; c4 < 4; ++c4) {
@@ -605,7 +618,7 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
                 }
             }
         }
-        if (p.lse != nullptr && row_ok)
+        if (p.lse != nullptr && row_ok && dev_check(head < p.ld / kD, p.status, kChkLse))
             p.lse[(size_t)head * (size_t)p.n + (size_t)row] = (m_used + log2f(l)) * 0.69314718055994531f;
         ++units;
     }

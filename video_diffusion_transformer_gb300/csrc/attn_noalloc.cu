@@ -64,6 +64,7 @@ fv_status setup_current_device(NoAllocDevice **out) {
 extern "C" fv_status fv_attn_fwd_noalloc(const void *Q, const void *K, const void *V, void *O, int64_t N, int H,
                                          int D, float scale, int head_group, float *lse, void *stream,
                                          int *device_status_out) {
+    fv::NvtxRange nvtx("fv_attn_fwd_noalloc");
     // the same checks as fv_attn_fwd, then the scratch limit
     fv_status st = fv::check_attn_args(Q, K, V, O, N, H, D, scale, head_group, lse);
     if (st != FV_OK) return st;
@@ -100,7 +101,7 @@ extern "C" fv_status fv_attn_fwd_noalloc(const void *Q, const void *K, const voi
             return FV_ERR_LAUNCH;
         fv_status dev_st = FV_OK;
         for (int i = 0; i < launches; ++i)
-            if (words[i] != 0) dev_st = FV_ERR_DEVICE_TIMEOUT;
+            if (words[i] != 0 && dev_st == FV_OK) dev_st = fv::status_of_word(words[i]);
         *device_status_out = (int)dev_st;
     }
     return FV_OK;

@@ -127,6 +127,13 @@ fv_status check_attn_args(const void *Q, const void *K, const void *V, const voi
     return FV_OK;
 }
 
+fv_status status_of_word(int word) {
+    if (word == 0) return FV_OK;
+    if ((word & 0xFF00) == kDevBadTag) return FV_ERR_ARG;
+    if ((word & 0xFF00) == kDevCheck) return FV_ERR_DEVICE_CHECK;
+    return FV_ERR_DEVICE_TIMEOUT;
+}
+
 int64_t take_test_skip_load(int kernel) {
     if (kernel < 0 || kernel >= kTestKernels) return -1;
     // a plain load first: launches with the hook disarmed never write the atomic
@@ -139,12 +146,14 @@ extern "C" {
 
 fv_status fv_attn_fwd(const void *Q, const void *K, const void *V, void *O, int64_t N, int H, int D, float scale,
                       int head_group, float *lse, void *stream) {
+    fv::NvtxRange nvtx("fv_attn_fwd");
     return attn_common(Q, K, V, O, N, H, D, scale, head_group, 0, 0, 0, lse, stream);
 }
 
 fv_status fv_attn_fwd_window(const void *Q, const void *K, const void *V, void *O, int64_t N, int H, int D,
                              float scale, int head_group, int frame_tokens, int chunk_frames, int window_chunks,
                              float *lse, void *stream) {
+    fv::NvtxRange nvtx("fv_attn_fwd_window");
     if (frame_tokens < 1 || chunk_frames < 1 || window_chunks < 0 || N < 1 || (N % frame_tokens) != 0) {
         if (!Q || !K || !V || !O) return FV_ERR_NULL;
         return FV_ERR_SHAPE;
@@ -156,6 +165,7 @@ fv_status fv_attn_fwd_window(const void *Q, const void *K, const void *V, void *
 fv_status fv_delta_attn(const void *Q, const void *K, const void *V, const float *beta, const float *alpha,
                         const float *text_state, int64_t N, int H, int D, int frame_tokens, int chunk_frames,
                         int window_chunks, void *O, float *states, float *workspace, void *stream) {
+    fv::NvtxRange nvtx("fv_delta_attn");
     if (!Q || !K || !V || !beta || !alpha || !O || !states || !workspace) return FV_ERR_NULL;
     if (D != 128 || N < 1 || N >= (int64_t(1) << 31) || H < 1 || H > 256 || frame_tokens < 1 ||
         (N % frame_tokens) != 0 || chunk_frames < 1 || window_chunks < 0)
@@ -209,6 +219,7 @@ int64_t fv_vsa_workspace_bytes(int H, int frames, int height, int width, int top
 fv_status fv_vsa_attn(const void *Q, const void *K, const void *V, void *O, int64_t N, int H, int D, float scale,
                       int frames, int height, int width, int topk, int32_t *selected, void *workspace,
                       int64_t workspace_bytes, float *lse, void *stream) {
+    fv::NvtxRange nvtx("fv_vsa_attn");
     if (!Q || !K || !V || !O || !selected || !workspace) return FV_ERR_NULL;
     if (D != 128 || H < 1 || H > 256 || frames < 4 || height < 4 || width < 4 || N < 1 ||
         N >= (int64_t(1) << 31) || N != (int64_t)frames * height * width)
@@ -261,6 +272,7 @@ fv_status fv_vsa_attn(const void *Q, const void *K, const void *V, void *O, int6
 fv_status fv_adaln_modulate(const void *x, void *y, int y_is_fp32, int64_t N, int C, const float *shift_table,
                             const float *scale_table, int64_t table_ld, int num_steps, int step, float eps,
                             void *stream) {
+    fv::NvtxRange nvtx("fv_adaln_modulate");
     if (!x || !y || !shift_table || !scale_table) return FV_ERR_NULL;
     if (N < 1 || C < 8 || C > 8192 || (C % 8) != 0 || table_ld < C || num_steps < 1) return FV_ERR_SHAPE;
     if (step < 0 || step >= num_steps) return FV_ERR_STEP;
@@ -280,6 +292,7 @@ fv_status fv_adaln_modulate(const void *x, void *y, int y_is_fp32, int64_t N, in
 
 fv_status fv_gated_residual(const void *x, const void *a, void *out, int64_t N, int C, const float *gate_table,
                             int64_t table_ld, int num_steps, int step, void *stream) {
+    fv::NvtxRange nvtx("fv_gated_residual");
     if (!x || !a || !out || !gate_table) return FV_ERR_NULL;
     if (N < 1 || C < 8 || C > (1 << 20) || (C % 8) != 0 || table_ld < C || num_steps < 1) return FV_ERR_SHAPE;
     if (step < 0 || step >= num_steps) return FV_ERR_STEP;
@@ -298,6 +311,7 @@ fv_status fv_gated_residual(const void *x, const void *a, void *out, int64_t N, 
 fv_status fv_adaln_modulate_tagged(const void *x, void *y, int y_is_fp32, int64_t N, int C, const float *shift_table,
                                    const float *scale_table, int64_t table_ld, int num_steps, int num_modalities,
                                    int step, const uint8_t *token_tags, float eps, void *stream) {
+    fv::NvtxRange nvtx("fv_adaln_modulate_tagged");
     if (!x || !y || !shift_table || !scale_table || !token_tags) return FV_ERR_NULL;
     if (N < 1 || C < 8 || C > 8192 || (C % 8) != 0 || table_ld < C || num_steps < 1 || num_modalities < 1 ||
         num_modalities > 255)
@@ -321,6 +335,7 @@ fv_status fv_adaln_modulate_tagged(const void *x, void *y, int y_is_fp32, int64_
 fv_status fv_gated_residual_tagged(const void *x, const void *a, void *out, int64_t N, int C, const float *gate_table,
                                    int64_t table_ld, int num_steps, int num_modalities, int step,
                                    const uint8_t *token_tags, void *stream) {
+    fv::NvtxRange nvtx("fv_gated_residual_tagged");
     if (!x || !a || !out || !gate_table || !token_tags) return FV_ERR_NULL;
     if (N < 1 || C < 8 || C > (1 << 20) || (C % 8) != 0 || table_ld < C || num_steps < 1 || num_modalities < 1 ||
         num_modalities > 255)
@@ -351,6 +366,7 @@ fv_status fv_step_for_timestep(const float *ladder, int num_steps, float t, int 
 }
 
 fv_status fv_sync_status(void *stream) {
+    fv::NvtxRange nvtx("fv_sync_status");
     DeviceState *d = nullptr;
     fv_status st = device_state(&d);
     if (st != FV_OK) return st;
@@ -363,7 +379,7 @@ fv_status fv_sync_status(void *stream) {
     if (word != 0) {
         if (cudaMemsetAsync(d->status, 0, sizeof(int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
             return FV_ERR_LAUNCH;
-        return (word & 0xFF00) == fv::kDevBadTag ? FV_ERR_ARG : FV_ERR_DEVICE_TIMEOUT;
+        return fv::status_of_word(word);
     }
     return FV_OK;
 }
@@ -380,6 +396,7 @@ const char *fv_status_string(fv_status s) {
         case FV_ERR_DEVICE_TIMEOUT: return "FV_ERR_DEVICE_TIMEOUT: a bounded wait inside a kernel ran out";
         case FV_ERR_ARG: return "FV_ERR_ARG: a scalar argument is invalid";
         case FV_ERR_ALIAS: return "FV_ERR_ALIAS: buffers overlap where the call forbids it";
+        case FV_ERR_DEVICE_CHECK: return "FV_ERR_DEVICE_CHECK: an in-kernel index check of the debug build failed";
     }
     return "unknown fv_status";
 }

@@ -4,17 +4,50 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
+
 #include <cstdint>
 
 #include "fv.h"
 
 namespace fv {
 
+// An NVTX range around one C-ABI call, named after the call, so a timeline
+// profiler shows which launches each call enqueued.  Without a profiler
+// attached the push and pop are calls to empty functions.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 // Device status word values (0 = no error).  A kernel that gives up on a
 // bounded wait stores kDevTimeout | where, where names the wait.
 constexpr int kDevTimeout = 0x7100;
 // A per-token modality tag was >= the number of modalities; the row was skipped.
 constexpr int kDevBadTag = 0x7200;
+// Debug build only: an in-kernel index check failed (kDevCheck | where); the
+// access it guarded was skipped.
+constexpr int kDevCheck = 0x7300;
+
+#ifndef FV_DEBUG_CHECKS
+#define FV_DEBUG_CHECKS 0
+#endif
+
+// Debug build: true when `ok`; otherwise records kDevCheck | where in the
+// status word (first error wins) and returns false, so the caller skips the
+// access.  Release build: always true, compiled out.
+__device__ __forceinline__ bool dev_check(bool ok, int *status, int where) {
+#if FV_DEBUG_CHECKS
+    if (!ok) atomicCAS(status, 0, kDevCheck | where);
+    return ok;
+#else
+    (void)status;
+    (void)where;
+    return true;
+#endif
+}
 
 // Compute capability check (10.3) and SM count of device `dev`; false if a
 // runtime query fails.
@@ -25,6 +58,9 @@ bool probe_device(int dev, bool *supported, int *num_sms);
 // the call returns without enqueueing anything.
 fv_status check_attn_args(const void *Q, const void *K, const void *V, const void *O, int64_t N, int H, int D,
                           float scale, int head_group, const float *lse);
+
+// The status a non-zero device status word stands for.
+fv_status status_of_word(int word);
 
 // The load index armed by fv_test_skip_load for `kernel` (an fv_test_kernel
 // value), or -1; reading it disarms the hook.

@@ -495,6 +495,10 @@ __device__ void producer(const CUtensorMap *tq, const Params &p, const Smem &sm,
             const uint32_t s = loads % kStages, ph = (loads / kStages) & 1u;
             if (!wait_bar(sm, kBarKvEmpty + (int)s, ph ^ 1u, p, kWhereKvEmpty)) return false;
             const int e0 = 2 * j < cnt ? lst[2 * j] : 0xFFFF, e1 = 2 * j + 1 < cnt ? lst[2 * j + 1] : 0xFFFF;
+            // debug build: every entry names a tile of the grid or no tile (0xFFFF)
+            dev_check(((e0 & 0xFFFF) < p.g.num_tiles || (e0 & 0xFFFF) == 0xFFFF) &&
+                          ((e1 & 0xFFFF) < p.g.num_tiles || (e1 & 0xFFFF) == 0xFFFF) && cnt <= p.list_ld,
+                      p.status, 0x12);
             const uint32_t full = sm.b(kBarKvFull + (int)(loads % kKvFullBars));
             if ((int64_t)loads != skipped) {
                 ptx::mbar_arrive_expect_tx(full, kTileBytes);
