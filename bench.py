@@ -633,7 +633,7 @@ def parse(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("fv", "reference"), default="fv")
     ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
-    ap.add_argument("--cpu-rows", type=int, default=96, help="oracle query rows per head for cpu_baseline")
+    ap.add_argument("--cpu-rows", type=int, default=256, help="oracle query rows per head for cpu_baseline")
     ap.add_argument("--ref-rows", type=int, default=16, help="oracle query rows per head per reference step")
     ap.add_argument("--cpu-ew-rows", type=int, default=8192,
                     help="rows of the oracle's modulate and gated residual timed alone for cpu_baseline")

@@ -8,7 +8,7 @@
 // arithmetic": the N x N scores are streamed, never stored).  Heads are
 // launched in groups (section "The rest is placement", item 1).
 //
-// Design (one persistent CTA per SM, 320 threads):
+// Design (one persistent CTA per SM, 384 threads):
 //   * work unit = (head, block of 256 query rows) = two 128-row q-tiles;
 //     units are dealt round-robin, heads outermost, so the CTAs running at
 //     the same time stream the same head's K/V through L2;
@@ -52,9 +52,20 @@ constexpr int kStages = 4;           // K/V ring slots
 constexpr int kHalfBytes = kRows * 64 * 2;   // one 128 x 64 bf16 half tile (16 KB)
 constexpr int kTileBytes = 2 * kHalfBytes;   // 32 KB
 constexpr int kSoftmaxWarps = 4 * kQTiles;
-constexpr int kTmaWarp = kSoftmaxWarps;
+constexpr int kTmaWarp = kSoftmaxWarps;      // warpgroup 2: TMA, MMA, two idle warps
 constexpr int kMmaWarp = kSoftmaxWarps + 1;
-constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
+// Register split (setmaxnreg).  The register file is divided among the SM's
+// four sub-partitions and a warp lives on sub-partition warp % 4, so with 10
+// or 12 warps some sub-partition holds three and every thread is capped at
+// 168 registers.  With 12 warps each sub-partition holds one softmax warp of
+// each q-tile and one warp of warpgroup 2; launched at 168 registers a thread
+// (12 x 32 x 168 = 64,512), warpgroup 2 moves to 120 and the softmax
+// warpgroups to 192 (2 x 192 + 120 = 3 x 168 per sub-partition lane), and
+// neither the softmax nor the TMA/MMA code spills.
+constexpr uint32_t kRegsLaunch = 168, kRegsSoftmax = 192, kRegsControl = 120;
+static_assert(2 * kRegsSoftmax + kRegsControl <= 3 * kRegsLaunch, "register split exceeds the launch total");
+static_assert(kThreads * kRegsLaunch <= 65536, "launch register total");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRedoSum = 1048576.0f;         // 2^20: largest tile sum kept against the reference max
 
@@ -670,11 +681,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
 
-    if (warp == kTmaWarp) {
-        if (lane == 0) producer<kWindow>(&tm_q, &tm_k, &tm_v, p, sm);
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) mma_issuer<kWindow>(p, sm, tmem);
+    if (warp >= kSoftmaxWarps) {
+        ptx::setmaxnreg_dec<kRegsControl>();
+        if (warp == kTmaWarp) {
+            if (lane == 0) producer<kWindow>(&tm_q, &tm_k, &tm_v, p, sm);
+        } else if (warp == kMmaWarp) {
+            if (lane == 0) mma_issuer<kWindow>(p, sm, tmem);
+        }
     } else {
+        ptx::setmaxnreg_inc<kRegsSoftmax>();
         softmax_role<kWindow>(p, sm, tmem, warp >> 2, (int)threadIdx.x & 127);
     }
     __syncwarp();  // lanes 1-31 of the TMA and MMA warps wait here for lane 0

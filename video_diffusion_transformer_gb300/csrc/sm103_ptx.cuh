@@ -207,6 +207,21 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
                  : "memory");
 }
 
+// ------------------------------------------------------ register split
+// Per-thread register limit of the calling warpgroup; every thread of the
+// warpgroup must execute it.  The block's register total stays the one it was
+// launched with: decrease in one warpgroup before another increases.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    static_assert(kRegs % 8 == 0 && kRegs >= 24 && kRegs <= 256, "setmaxnreg range");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    static_assert(kRegs % 8 == 0 && kRegs >= 24 && kRegs <= 256, "setmaxnreg range");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ------------------------------------------------------------------ math
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
