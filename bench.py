@@ -591,12 +591,15 @@ def run_fv(args):
     # burst figure is the denominator, the sustained ratio a second field.
     peak = pk["bf16_tflops"]
     sustained = pk["bf16_tflops_sustained"]
+    # DRAM bytes of the step's attention launches, from one ncu capture of a
+    # single 16-head launch of this workload (a step's 16-head launches are the
+    # same launch), scaled by heads; null once the kernel source has changed.
     traffic = None
     prof = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(prof):
         rec = json.load(open(prof)).get(w.name)
         if rec and rec.get("kernel_source") == attn_source_hash():
-            traffic = rec["attn_fwd_kernel_bytes_per_step"]
+            traffic = rec["attn_fwd_kernel_bytes"] * w.heads / rec["heads_captured"]
     value = world * w.flops * args.steps / (ms_total / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
