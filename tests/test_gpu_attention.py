@@ -64,6 +64,24 @@ def test_workload_sampled_rows(name):
     P.assert_attention_ok(err)
 
 
+def test_maximum_head_count():
+    """H = 256, the largest head count the ABI takes, at a ragged length: one
+    launch of all heads, ragged groups of 7 and one head per launch give the
+    same bits, and every head matches the oracle (sampled heads across the
+    range, all rows)."""
+    n, heads = 300, 256
+    q, k, v = rand(n, heads, 256)
+    outs = []
+    for hg in (256, 7, 1):
+        o, lse = run(q, k, v, heads, hg)
+        outs.append((o, lse))
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+    o, lse = outs[0]
+    err = P.attention_errors(q, k, v, o, heads, 0, SCALE, lse, head_list=[0, 1, 100, 127, 128, 200, 254, 255])
+    P.assert_attention_ok(err)
+
+
 def test_head_grouping_does_not_change_results():
     n, heads = 3000, 6
     q, k, v = rand(n, heads, 7)

@@ -10,11 +10,13 @@
 //
 // vda_stats_tc (persistent, one CTA per SM, 448 threads): unit = (frame, head).
 //   warp 12 (one thread): TMA loads of 64-token stages, K and V as 64 x 64
-//     bf16 boxes in the 128-byte swizzled layout, two stages in flight;
+//     bf16 boxes in the 128-byte swizzled layout, into a ring of four raw
+//     stages, so up to four stages of loads are in flight;
 //   warps 4-11 (the scalers): thread = (token, channel quarter); squared norm
 //     of k over the four quarters, then w_A k and w_B v split into hi and lo,
 //     written to the same (swizzled) byte positions of their own buffers (v's
-//     hi over v itself), so every operand shares K's layout;
+//     hi over v itself in the raw stage, the other three in a ring of two
+//     scaled stages), so every operand shares K's layout;
 //   warp 13 (one thread): per 16 tokens, D_A += K^T (w_A K)_hi, D_A += K^T
 //     (w_A K)_lo, D_B += (w_B V)_hi^T K, D_B += (w_B V)_lo^T K, both operands
 //     MN-major (channels contiguous); D_A and D_B in tensor memory, double
@@ -40,10 +42,15 @@ constexpr int kD = 128;
 constexpr int kTok = 64;                       // tokens per stage
 constexpr int kHalf = kTok * 64 * 2;           // one 64-token x 64-channel box (8 KB)
 constexpr int kOperand = 2 * kHalf;            // 64 tokens x 128 channels (16 KB)
-// stage layout: K, V (overwritten by (w_B V)_hi), (w_B V)_lo, (w_A K)_hi, (w_A K)_lo
-constexpr int kOffK = 0, kOffVHi = kOperand, kOffVLo = 2 * kOperand, kOffXHi = 3 * kOperand, kOffXLo = 4 * kOperand;
-constexpr int kStageBytes = 5 * kOperand;      // 80 KB
-constexpr int kStages = 2;
+// raw stage: K, V (overwritten by (w_B V)_hi); scaled stage: (w_B V)_lo,
+// (w_A K)_hi, (w_A K)_lo.  A raw stage is free once its MMAs completed, a
+// scaled stage too; the scalers fill scaled stage g % 2 from raw stage g % 4.
+constexpr int kOffK = 0, kOffVHi = kOperand;                        // in a raw stage
+constexpr int kOffVLo = 0, kOffXHi = kOperand, kOffXLo = 2 * kOperand;  // in a scaled stage
+constexpr int kRawBytes = 2 * kOperand;        // 32 KB
+constexpr int kScaledBytes = 3 * kOperand;     // 48 KB
+constexpr int kStages = 4;                     // raw stages (loads in flight)
+constexpr int kScaled = 2;                     // scaled stages
 constexpr int kThreads = 448;
 constexpr int kScalers = 256;                  // warps 4-11: 64 tokens x 4 channel quarters
 constexpr int kTmaWarp = 12, kMmaWarp = 13;
@@ -51,20 +58,22 @@ constexpr uint32_t kTmemCols = 512;            // 2 buffers x (D_A, D_B)
 
 constexpr int kBarKvFull = 0;                  // TMA -> scalers
 constexpr int kBarXFull = kBarKvFull + kStages;     // scalers -> MMA (256 arrivals)
-constexpr int kBarStageEmpty = kBarXFull + kStages;  // MMA -> producer
-constexpr int kBarAccFull = kBarStageEmpty + kStages;  // MMA -> epilogue
+constexpr int kBarStageEmpty = kBarXFull + kScaled;  // MMA -> producer (raw stage free)
+constexpr int kBarXEmpty = kBarStageEmpty + kStages;  // MMA -> scalers (scaled stage free)
+constexpr int kBarAccFull = kBarXEmpty + kScaled;  // MMA -> epilogue
 constexpr int kBarAccEmpty = kBarAccFull + 2;  // epilogue -> MMA (128 arrivals)
 constexpr int kBarDrain = kBarAccEmpty + 2;
 constexpr int kNumBars = kBarDrain + 1;
 
-constexpr int kSmemStages = 0;
-constexpr int kSmemBar = kSmemStages + kStages * kStageBytes;
+constexpr int kSmemStages = 0;                                   // raw stages
+constexpr int kSmemScaled = kSmemStages + kStages * kRawBytes;   // scaled stages
+constexpr int kSmemBar = kSmemScaled + kScaled * kScaledBytes;
 constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
 constexpr int kSmemBytes = kSmemMisc + 16 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 constexpr int kWhereStageEmpty = 1, kWhereKvFull = 2, kWhereXFull = 3, kWhereAccEmpty = 4, kWhereAccFull = 5,
-              kWhereDrain = 6;
+              kWhereDrain = 6, kWhereXEmpty = 7;
 
 struct Params {
     const float *beta;  // [heads, n]
@@ -77,7 +86,7 @@ struct Params {
 };
 
 struct Smem {
-    uint32_t stages, bar;
+    uint32_t stages, scaled, bar;
     volatile int *abort_flag;
     __device__ uint32_t b(int i) const { return bar + 8u * (uint32_t)i; }
 };
@@ -111,7 +120,7 @@ __device__ void producer(const CUtensorMap *tk, const CUtensorMap *tv, const Par
             const uint32_t slot = g % kStages;
             ok = wait_bar(sm, kBarStageEmpty + (int)slot, ((g / kStages) & 1u) ^ 1u, p, kWhereStageEmpty);
             if (!ok) break;
-            const uint32_t base = sm.stages + slot * (uint32_t)kStageBytes;
+            const uint32_t base = sm.stages + slot * (uint32_t)kRawBytes;
             const int row = frame * p.frame_tokens + s * kTok;
             if ((int64_t)g == skipped) continue;
             ptx::mbar_arrive_expect_tx(sm.b(kBarKvFull + (int)slot), 2 * kOperand);
@@ -149,7 +158,7 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_
 // an offset that makes the eight lanes of a quarter-warp (two tokens, four
 // quarters) read eight different positions, i.e. eight bank groups.  The
 // swizzle does not matter here: a position is read and written in place.
-__device__ void scaler(const Params &p, const Smem &sm, uint8_t *smem_stages, int t) {
+__device__ void scaler(const Params &p, const Smem &sm, uint8_t *smem_stages, uint8_t *smem_scaled, int t) {
     const int u = t >> 2, c = t & 3;
     const int rot = 2 * (c >> 1) + u;
     uint32_t g = 0;
@@ -158,14 +167,19 @@ __device__ void scaler(const Params &p, const Smem &sm, uint8_t *smem_stages, in
         int frame, head;
         unit_of(p, unit, frame, head);
         for (int s = 0; ok && s < p.stages; ++s, ++g) {
-            const uint32_t slot = g % kStages;
+            const uint32_t slot = g % kStages, xs = g % kScaled;
             const int tok = s * kTok + u;  // token within the frame
             const float beta = tok < p.frame_tokens
                                    ? p.beta[(size_t)head * p.n + (size_t)frame * p.frame_tokens + tok]
                                    : 0.0f;
             ok = __all_sync(0xffffffffu, wait_bar(sm, kBarKvFull + (int)slot, (g / kStages) & 1u, p, kWhereKvFull));
             if (!ok) break;
-            uint8_t *st = smem_stages + (size_t)slot * kStageBytes;
+            // the scaled stage's previous MMAs (stage g - 2) are done with it
+            ok = __all_sync(0xffffffffu,
+                            wait_bar(sm, kBarXEmpty + (int)xs, ((g / kScaled) & 1u) ^ 1u, p, kWhereXEmpty));
+            if (!ok) break;
+            uint8_t *st = smem_stages + (size_t)slot * kRawBytes;
+            uint8_t *sc = smem_scaled + (size_t)xs * kScaledBytes;
             const int row_off = (c >> 1) * kHalf + u * 128;
             uint4 kc[4];
             float ss = 0.f;
@@ -199,28 +213,29 @@ __device__ void scaler(const Params &p, const Smem &sm, uint8_t *smem_stages, in
                     split2(wa * kf.x, wa * kf.y, xh[e], xl[e]);
                     split2(wb * vf.x, wb * vf.y, vh[e], vl[e]);
                 }
-                *reinterpret_cast<uint4 *>(st + kOffXHi + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
-                *reinterpret_cast<uint4 *>(st + kOffXLo + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
+                *reinterpret_cast<uint4 *>(sc + kOffXHi + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+                *reinterpret_cast<uint4 *>(sc + kOffXLo + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
                 *reinterpret_cast<uint4 *>(st + kOffVHi + off) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
-                *reinterpret_cast<uint4 *>(st + kOffVLo + off) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
+                *reinterpret_cast<uint4 *>(sc + kOffVLo + off) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
             }
             // the tensor core reads these through the async proxy
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            ptx::mbar_arrive(sm.b(kBarXFull + (int)slot));
+            ptx::mbar_arrive(sm.b(kBarXFull + (int)xs));
         }
     }
 }
 
-constexpr uint64_t kDescStage = (uint64_t)(kStageBytes >> 4);
+constexpr uint64_t kDescRaw = (uint64_t)(kRawBytes >> 4);
+constexpr uint64_t kDescScaled = (uint64_t)(kScaledBytes >> 4);
 
 __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
     // MN-major operands: channel halves 8 KB apart (leading offset), 8-token
     // groups 1 KB apart (stride offset); 16 tokens per MMA = 2 KB
     const uint64_t dk = ptx::sdesc_sw128(sm.stages + kOffK, kHalf, 1024);
     const uint64_t dvh = ptx::sdesc_sw128(sm.stages + kOffVHi, kHalf, 1024);
-    const uint64_t dvl = ptx::sdesc_sw128(sm.stages + kOffVLo, kHalf, 1024);
-    const uint64_t dxh = ptx::sdesc_sw128(sm.stages + kOffXHi, kHalf, 1024);
-    const uint64_t dxl = ptx::sdesc_sw128(sm.stages + kOffXLo, kHalf, 1024);
+    const uint64_t dvl = ptx::sdesc_sw128(sm.scaled + kOffVLo, kHalf, 1024);
+    const uint64_t dxh = ptx::sdesc_sw128(sm.scaled + kOffXHi, kHalf, 1024);
+    const uint64_t dxl = ptx::sdesc_sw128(sm.scaled + kOffXLo, kHalf, 1024);
     constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, true, true);
     uint32_t g = 0, units = 0;
     bool ok = true;
@@ -231,21 +246,22 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
         ptx::tc_fence_after();
         const uint32_t d_a = tmem + 256u * buf, d_b = d_a + 128u;
         for (int s = 0; ok && s < p.stages; ++s, ++g) {
-            const uint32_t slot = g % kStages;
-            ok = wait_bar(sm, kBarXFull + (int)slot, (g / kStages) & 1u, p, kWhereXFull);
+            const uint32_t slot = g % kStages, xs = g % kScaled;
+            ok = wait_bar(sm, kBarXFull + (int)xs, (g / kScaled) & 1u, p, kWhereXFull);
             if (!ok) break;
             ptx::tc_fence_after();
-            const uint64_t so = slot * kDescStage;
+            const uint64_t ro = slot * kDescRaw, so = xs * kDescScaled;
 #pragma unroll
             for (int kk = 0; kk < kTok / 16; ++kk) {
-                const uint64_t off = so + (uint64_t)((kk * 16 * 128) >> 4);
+                const uint64_t off = (uint64_t)((kk * 16 * 128) >> 4);
                 const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-                ptx::mma_ss(d_a, dk + off, dxh + off, idesc, acc);
-                ptx::mma_ss(d_a, dk + off, dxl + off, idesc, 1u);
-                ptx::mma_ss(d_b, dvh + off, dk + off, idesc, acc);
-                ptx::mma_ss(d_b, dvl + off, dk + off, idesc, 1u);
+                ptx::mma_ss(d_a, dk + ro + off, dxh + so + off, idesc, acc);
+                ptx::mma_ss(d_a, dk + ro + off, dxl + so + off, idesc, 1u);
+                ptx::mma_ss(d_b, dvh + ro + off, dk + ro + off, idesc, acc);
+                ptx::mma_ss(d_b, dvl + so + off, dk + ro + off, idesc, 1u);
             }
             ptx::tc_commit(sm.b(kBarStageEmpty + (int)slot));
+            ptx::tc_commit(sm.b(kBarXEmpty + (int)xs));
         }
         if (!ok) break;
         ptx::tc_commit(sm.b(kBarAccFull + (int)buf));
@@ -300,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + (base - raw);
     Smem sm;
     sm.stages = base + kSmemStages;
+    sm.scaled = base + kSmemScaled;
     sm.bar = base + kSmemBar;
     sm.abort_flag = reinterpret_cast<volatile int *>(smem + kSmemMisc + 4);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + kSmemMisc);
@@ -307,8 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(sm.b(kBarKvFull + s), 1);
-            ptx::mbar_init(sm.b(kBarXFull + s), kScalers);
             ptx::mbar_init(sm.b(kBarStageEmpty + s), 1);
+        }
+        for (int s = 0; s < kScaled; ++s) {
+            ptx::mbar_init(sm.b(kBarXFull + s), kScalers);
+            ptx::mbar_init(sm.b(kBarXEmpty + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(sm.b(kBarAccFull + b), 1);
@@ -335,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         if (lane == 0) mma_issuer(p, sm, tmem);
     } else if (warp >= 4) {
-        scaler(p, sm, smem + kSmemStages, (int)threadIdx.x - 128);
+        scaler(p, sm, smem + kSmemStages, smem + kSmemScaled, (int)threadIdx.x - 128);
     } else {
         epilogue(p, sm, tmem, (int)threadIdx.x);
     }
