@@ -187,15 +187,25 @@ __device__ __forceinline__ uint32_t score_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// The k-th largest key of keys[0, n), found bit by bit by one warp.
+// The k-th largest key of keys[0, n), found bit by bit by one warp.  Each
+// pass counts the keys at or above a candidate; the count runs four
+// independent loads per lane at a time (one shared-memory load in flight per
+// lane made every pass a chain of ~38 load latencies).
 __device__ uint32_t kth_largest_key(const uint32_t *keys, int n, int k, int lane) {
     uint32_t t = 0;
     for (int b = 31; b >= 0; --b) {
         const uint32_t cand = t | (1u << b);
-        int cnt = 0;
-        for (int i = lane; i < n; i += 32) cnt += keys[i] >= cand ? 1 : 0;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+        int i = lane;
+        for (; i + 96 < n; i += 128) {
+            const uint32_t k0 = keys[i], k1 = keys[i + 32], k2 = keys[i + 64], k3 = keys[i + 96];
+            c0 += k0 >= cand ? 1 : 0;
+            c1 += k1 >= cand ? 1 : 0;
+            c2 += k2 >= cand ? 1 : 0;
+            c3 += k3 >= cand ? 1 : 0;
+        }
+        for (; i < n; i += 32) c0 += keys[i] >= cand ? 1 : 0;
+        const int cnt = (int)__reduce_add_sync(0xffffffffu, (unsigned)((c0 + c1) + (c2 + c3)));
         if (cnt >= k) t = cand;
     }
     return t;
