@@ -162,8 +162,9 @@ fv_status fv_attn_fwd_window(const void *Q, const void *K, const void *V, void *
  * normalised keys, values, the inverse (I + A_t)^{-1}, the scanned
  * S Diag(alpha) + B, the summed states) are split into bf16 hi + lo parts, so
  * the products keep close to float32 accuracy (states within ~2e-5 relative
- * of float64 over 72 frames).  The per-frame inversion (Gauss-Jordan on
- * I + A_t, symmetric positive definite) runs in float32.  O is rounded once
+ * of float64 over 72 frames).  The per-frame inversion (a symmetric sweep,
+ * i.e. Gauss-Jordan elimination kept symmetric, on I + A_t, symmetric
+ * positive definite) runs in float32.  O is rounded once
  * to bf16.
  */
 fv_status fv_delta_attn(const void *Q, const void *K, const void *V, const float *beta,
