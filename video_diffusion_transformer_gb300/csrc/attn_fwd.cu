@@ -19,6 +19,13 @@
 //     K-major in shared memory) and O_k += P_k V_j (P from tensor memory, V
 //     MN-major in shared memory), ping-ponging between the two q-tiles so the
 //     tensor core works on one tile while the other tile's softmax runs;
+//   * warp 10 (one thread) takes the data waits off the MMA thread: it waits
+//     until V_j and K_j+1 have landed and adds its arrival to each q-tile's
+//     P barrier, so the MMA thread checks one barrier before each q-tile's
+//     P V_j + Q K_j+1^T batch.  A barrier check between two MMA batches
+//     leaves the tensor pipe idle for about as long as one MMA (the issuing
+//     thread runs only about one MMA ahead), so every check removed from the
+//     issuing thread is pipe time won;
 //   * warps 0-3 and 4-7 are the softmax warpgroups of q-tile 0 and 1: thread
 //     t owns query row t (TMEM lane t).  Per K/V tile it reads its 128 scores
 //     from TMEM, writes p = 2^(s*scale*log2e - m) as bf16 back over the
@@ -52,8 +59,9 @@ constexpr int kStages = 4;           // K/V ring slots
 constexpr int kHalfBytes = kRows * 64 * 2;   // one 128 x 64 bf16 half tile (16 KB)
 constexpr int kTileBytes = 2 * kHalfBytes;   // 32 KB
 constexpr int kSoftmaxWarps = 4 * kQTiles;
-constexpr int kTmaWarp = kSoftmaxWarps;      // warpgroup 2: TMA, MMA, two idle warps
+constexpr int kTmaWarp = kSoftmaxWarps;      // warpgroup 2: TMA, MMA, the watcher, one idle warp
 constexpr int kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kWatchWarp = kSoftmaxWarps + 2;   // waits for V_j and K_j+1 on the MMA thread's behalf
 constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
 // Register split (setmaxnreg).  The register file is divided among the SM's
 // four sub-partitions and a warp lives on sub-partition warp % 4, so with 10
@@ -362,8 +370,6 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
             const uint32_t iv = ring + 2u * (uint32_t)j + 1u, sv = iv % kStages;
             const uint32_t ik = iv + 1u, sk = ik % kStages;
             const bool more = j + 1 < n_kv;
-            ok = wait_bar(sm, kBarKvFull + (int)sv, (iv / kStages) & 1u, p, kWhereKvFull);
-            if (!ok) break;
             const uint64_t vdesc = dsc.v0 + sv * kDescTile;
             const uint64_t kdesc = dsc.kv0 + sk * kDescTile;
 #pragma unroll
@@ -375,11 +381,6 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
                 if (k == kQTiles - 1) ptx::tc_commit(sm.b(kBarKvEmpty + (int)sv));
                 if (!more) ptx::tc_commit(sm.b(kBarOFull + k));
                 if (more) {
-                    if (k == 0) {
-                        ok = wait_bar(sm, kBarKvFull + (int)sk, (ik / kStages) & 1u, p, kWhereKvFull);
-                        if (!ok) break;
-                        ptx::tc_fence_after();
-                    }
                     issue_qk(tmem + (uint32_t)(128 * k), dsc.q0 + (uint64_t)k * kDescTile, kdesc);
                     ptx::tc_commit(sm.b(kBarSFull + k));
                     if (k == kQTiles - 1) ptx::tc_commit(sm.b(kBarKvEmpty + (int)sk));
@@ -395,6 +396,34 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
     // Every MMA issued must complete before the tensor memory is released.
     ptx::tc_commit(sm.b(kBarDrain));
     drain_bar(sm, kBarDrain, 0u, p);
+}
+
+// -------------------------------------------------------------- watcher
+// The MMA thread's data waits, taken off its issue path: for K/V tile j of a
+// unit the watcher waits until V_j and K_j+1 have landed and then adds its
+// arrival to each q-tile's P barrier, so that barrier's phase j completes
+// only when the softmax has stored P_j and the MMAs after it have their
+// operands.  It arrives for tile j + 1 only once phase j is complete.
+template <bool kWindow>
+__device__ void watcher(const Params &p, const Smem &sm) {
+    uint32_t ring = 0, tile = 0;
+    bool ok = true;
+    int head_off = 0, qb = 0;
+    for (int i = 0; ok && unit_at<kWindow>(p, i, head_off, qb); ++i) {
+        const int n_kv = kv_list<kWindow>(p, qb).count;
+        for (int j = 0; ok && j < n_kv; ++j) {
+            const uint32_t iv = ring + 2u * (uint32_t)j + 1u, ik = iv + 1u;
+            ok = wait_bar(sm, kBarKvFull + (int)(iv % kStages), (iv / kStages) & 1u, p, kWhereKvFull);
+            if (ok && j + 1 < n_kv)
+                ok = wait_bar(sm, kBarKvFull + (int)(ik % kStages), (ik / kStages) & 1u, p, kWhereKvFull);
+            for (int k = 0; ok && k < kQTiles; ++k) {
+                if (tile > 0) ok = wait_bar(sm, kBarPFull + k, (tile - 1u) & 1u, p, kWherePFull);
+                if (ok) ptx::mbar_arrive(sm.b(kBarPFull + k));
+            }
+            ++tile;
+        }
+        ring += 2u * (uint32_t)n_kv;
+    }
 }
 
 // -------------------------------------------------------------- softmax
@@ -660,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(sm.b(kBarQEmpty), 1);
         for (int k = 0; k < kQTiles; ++k) {
             ptx::mbar_init(sm.b(kBarSFull + k), 1);
-            ptx::mbar_init(sm.b(kBarPFull + k), 128);
+            ptx::mbar_init(sm.b(kBarPFull + k), 128 + 1);   // softmax threads + the watcher
             ptx::mbar_init(sm.b(kBarOFull + k), 1);
         }
         ptx::mbar_init(sm.b(kBarDrain), 1);
@@ -687,6 +716,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) producer<kWindow>(&tm_q, &tm_k, &tm_v, p, sm);
         } else if (warp == kMmaWarp) {
             if (lane == 0) mma_issuer<kWindow>(p, sm, tmem);
+        } else if (warp == kWatchWarp) {
+            if (lane == 0) watcher<kWindow>(p, sm);
         }
     } else {
         ptx::setmaxnreg_inc<kRegsSoftmax>();
