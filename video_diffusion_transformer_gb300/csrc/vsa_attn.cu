@@ -246,23 +246,32 @@ __global__ void __launch_bounds__(256, 1)
     }
     __syncthreads();
     const int rows = 2 * np;
-    for (int c = tid; c < nt; c += (int)blockDim.x) {
+    // a thread scores key tiles c and c + blockDim.x together, so each query
+    // mean read from shared memory feeds both (the second tile repeats the
+    // first past the end; its scores are not stored)
+    for (int c = tid; c < nt; c += 2 * (int)blockDim.x) {
+        const int c2 = c + (int)blockDim.x < nt ? c + (int)blockDim.x : c;
         const float4 *kr = reinterpret_cast<const float4 *>(kbar + ((size_t)h * nt + c) * kD);
-        float acc[kSelMaxRows];
+        const float4 *kr2 = reinterpret_cast<const float4 *>(kbar + ((size_t)h * nt + c2) * kD);
+        float acc[kSelMaxRows], acc2[kSelMaxRows];
 #pragma unroll
-        for (int r = 0; r < kSelMaxRows; ++r) acc[r] = 0.f;
-#pragma unroll 4
+        for (int r = 0; r < kSelMaxRows; ++r) acc[r] = 0.f, acc2[r] = 0.f;
+#pragma unroll 2
         for (int d4 = 0; d4 < kD / 4; ++d4) {
-            const float4 kk = kr[d4];
+            const float4 kk = kr[d4], kk2 = kr2[d4];
 #pragma unroll
             for (int r = 0; r < kSelMaxRows; ++r) {
                 const float4 qq = *reinterpret_cast<const float4 *>(qs + r * kD + 4 * d4);
                 acc[r] = fmaf(qq.x, kk.x, fmaf(qq.y, kk.y, fmaf(qq.z, kk.z, fmaf(qq.w, kk.w, acc[r]))));
+                acc2[r] = fmaf(qq.x, kk2.x, fmaf(qq.y, kk2.y, fmaf(qq.z, kk2.z, fmaf(qq.w, kk2.w, acc2[r]))));
             }
         }
 #pragma unroll
         for (int r = 0; r < kSelMaxRows; ++r)
-            if (r < rows) keys[r * nt + c] = score_key(acc[r]);
+            if (r < rows) {
+                keys[r * nt + c] = score_key(acc[r]);
+                if (c2 != c) keys[r * nt + c2] = score_key(acc2[r]);
+            }
     }
     __syncthreads();
     for (int r = warp; r < rows; r += 8) {
