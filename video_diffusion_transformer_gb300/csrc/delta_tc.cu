@@ -971,11 +971,13 @@ __device__ void rows(const Params &p, const Smem &sm, uint32_t tmem, int h, int 
             stage_row(sm, r, qg, v);
             if (s < steps) form_u(v, al, bn, q, qg, t_hi, t_lo);
         }
-        // the last written state also goes to the far anchor frame
-        write_rows(sm, r, ch, out + (size_t)tf * kD * kD, s == steps ? out + (size_t)last * kD * kD : nullptr);
+        // U_{s+1} is in tensor memory and S_s staged: the next step's MMAs may
+        // start (they overwrite D) while S_s goes out to global memory
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(sm.b(kBarA));
+        // the last written state also goes to the far anchor frame
+        write_rows(sm, r, ch, out + (size_t)tf * kD * kD, s == steps ? out + (size_t)last * kD * kD : nullptr);
     }
 }
 
