@@ -403,7 +403,14 @@ __device__ void mma_issuer(const Params &p, const Smem &sm, uint32_t tmem) {
 // unit the watcher waits until V_j and K_j+1 have landed and then adds its
 // arrival to each q-tile's P barrier, so that barrier's phase j completes
 // only when the softmax has stored P_j and the MMAs after it have their
-// operands.  It arrives for tile j + 1 only once phase j is complete.
+// operands.  Order, per tile j: phase j - 1 of q-tile 0's P barrier complete
+// (S_0 of tile j - 1 was computed, so K_j-1, the previous load in K_j+1's
+// slot, has landed; V_j's slot last held V_j-2, which this thread waited
+// for), then V_j and K_j+1, then the arrival for q-tile 0, then phase j - 1
+// of q-tile 1's barrier and its arrival.  The unit's K_0 is the MMA thread's
+// own wait.  No slot is refilled before this thread's arrival for the load in
+// it (its consumer, P V_j or Q K_j+1^T, waits for that arrival), so no parity
+// wait here can meet a barrier two phases on.
 template <bool kWindow>
 __device__ void watcher(const Params &p, const Smem &sm) {
     uint32_t ring = 0, tile = 0;
@@ -413,10 +420,13 @@ __device__ void watcher(const Params &p, const Smem &sm) {
         const int n_kv = kv_list<kWindow>(p, qb).count;
         for (int j = 0; ok && j < n_kv; ++j) {
             const uint32_t iv = ring + 2u * (uint32_t)j + 1u, ik = iv + 1u;
-            ok = wait_bar(sm, kBarKvFull + (int)(iv % kStages), (iv / kStages) & 1u, p, kWhereKvFull);
+            if (tile > 0) ok = wait_bar(sm, kBarPFull + 0, (tile - 1u) & 1u, p, kWherePFull);
+            if (ok) ok = wait_bar(sm, kBarKvFull + (int)(iv % kStages), (iv / kStages) & 1u, p, kWhereKvFull);
             if (ok && j + 1 < n_kv)
                 ok = wait_bar(sm, kBarKvFull + (int)(ik % kStages), (ik / kStages) & 1u, p, kWhereKvFull);
-            for (int k = 0; ok && k < kQTiles; ++k) {
+            if (!ok) break;
+            ptx::mbar_arrive(sm.b(kBarPFull + 0));
+            for (int k = 1; ok && k < kQTiles; ++k) {
                 if (tile > 0) ok = wait_bar(sm, kBarPFull + k, (tile - 1u) & 1u, p, kWherePFull);
                 if (ok) ptx::mbar_arrive(sm.b(kBarPFull + k));
             }
