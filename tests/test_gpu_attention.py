@@ -82,6 +82,23 @@ def test_maximum_head_count():
     P.assert_attention_ok(err)
 
 
+@pytest.mark.parametrize("n", [100, 128, 129])
+def test_many_short_units_per_cta(n):
+    """256 heads of at most two K/V tiles in one launch: each CTA runs one
+    (head, query block) unit after another with one or two K/V tiles each,
+    so the ring of K/V slots, the P barriers and the thread that waits for
+    the loads on the MMA thread's behalf cross unit boundaries every tile or
+    two.  Every sampled head matches the oracle on all rows, and one head
+    per launch gives the same bits."""
+    heads = 256
+    q, k, v = rand(n, heads, 400 + n)
+    o, lse = run(q, k, v, heads, heads)
+    o1, lse1 = run(q, k, v, heads, 1)
+    assert torch.equal(o, o1) and torch.equal(lse, lse1)
+    err = P.attention_errors(q, k, v, o, heads, 0, SCALE, lse, head_list=[0, 1, 151, 152, 153, 200, 255])
+    P.assert_attention_ok(err)
+
+
 def test_head_grouping_does_not_change_results():
     n, heads = 3000, 6
     q, k, v = rand(n, heads, 7)
