@@ -69,6 +69,26 @@ def test_no_text_state_and_short_clips():
         assert ws <= 1e-4 and wo <= 1e-2
 
 
+def test_aligned_keys_make_ill_conditioned_frames():
+    """Every key of a frame close to one direction and beta = 1: I + A_t has
+    one eigenvalue near the frame's token count (256) and the rest near 1,
+    so the per-frame inverse is ill-conditioned (~257) and its pivots span
+    that range.  States and readout stay within the same bounds as the
+    well-conditioned cases."""
+    frames, t, heads = 8, 256, 2
+    q, k, v, beta, alpha, ts = make(frames, t, heads, 901)
+    g = torch.Generator().manual_seed(902)
+    for h in range(heads):
+        u = torch.randn(128, generator=g)
+        noise = 0.05 * torch.randn((frames * t, 128), generator=g)
+        k[:, h * 128:(h + 1) * 128] = (u[None, :] + noise).to(torch.bfloat16)
+    beta = torch.ones_like(beta)
+    ws, wo = check(q, k, v, beta, alpha, ts, t, 2, 1)
+    print(f"aligned keys: worst state error {ws:.3g}, worst output error {wo:.3g}")
+    assert ws <= 1e-3, ws
+    assert wo <= 1e-2, wo
+
+
 def test_no_writes_is_pure_decay():
     frames, t = 10, 32
     q, k, v, beta, alpha, ts = make(frames, t, 2, 7)
