@@ -146,6 +146,8 @@ __global__ void __launch_bounds__(256)
         float sq[8], sk[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) sq[e] = sk[e] = 0.f;
+        // four tokens' loads in flight per thread (one at a time left HBM at 81 %)
+#pragma unroll 4
         for (int r = 0; r < kTok; ++r) {
             const int lt = r >> 4, lh = (r >> 2) & 3, lw = r & 3;
             uint4 kk = make_uint4(0u, 0u, 0u, 0u), vv = make_uint4(0u, 0u, 0u, 0u);
