@@ -494,8 +494,35 @@ def run_fv(args):
                         "gbs_best": nbytes / best / 1e6,
                         "frac_of_hbm_median": (nbytes / med / 1e6) / hbm if hbm else None}
 
+            # the small configurations' operands (1,008 rows of modulate, 5,040 of
+            # the gated residual, <= 163 MB) stay in L2 between reps: timed
+            # without the flush and labelled so
+            def time_resident(fn, reps=20):
+                fn()
+                times = []
+                for _ in range(reps):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                    e1.synchronize()
+                    times.append(e0.elapsed_time(e1))
+                return statistics.median(times), min(times)
+
+            rm = W.tokens_per_latent_frame(1344, 768)   # 1,008 rows: one latent frame
+            rg = 5 * rm                                  # 5,040 rows: one 17-frame VAE chunk
+            with torch.cuda.stream(stream):
+                mod_s = time_resident(lambda: fv.adaln_modulate(ex[:rm], shift, scale, W.ADALN_STEP, eps=EPS,
+                                                                out=ey[:rm], stream=stream))
+                gre_s = time_resident(lambda: fv.gated_residual(ex[:rg], ea[:rg], gate, W.ADALN_STEP, out=eo[:rg],
+                                                                stream=stream))
+            fv.sync_status(stream)
+            resident = {"flush": "none: the operands stay in L2 (labelled L2-resident)", "reps": 20,
+                        "adaln_modulate_bf16": dict(entry(mod_s, rm * W.HIDDEN * 4 + 2 * W.HIDDEN * 4), rows=rm),
+                        "gated_residual": dict(entry(gre_s, rg * W.HIDDEN * 6 + W.HIDDEN * 4), rows=rg)}
             elementwise = {"rows": rows, "hidden": W.HIDDEN, "flush": "512 MB written before every rep",
                            "reps": 20, "peak_gbs": hbm, "adaln_modulate_bf16": entry(mod, mod_bytes),
+                           "l2_resident_small": resident,
                            "gated_residual": entry(gre, gre_bytes),
                            "tagged": {"modalities": nmod, "tags": "one per token, seeded uniform",
                                       "adaln_modulate_bf16": entry(mod_t, rows * W.HIDDEN * 4 + rows
