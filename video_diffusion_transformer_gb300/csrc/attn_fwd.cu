@@ -42,8 +42,12 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <numeric>
+#include <queue>
+#include <vector>
 
 #include "fv_internal.h"
 #include "sm103_ptx.cuh"
@@ -102,7 +106,8 @@ constexpr int kWhereQEmpty = 1, kWhereKvEmpty = 2, kWhereQFull = 3, kWhereKvFull
               kWhereSFull = 6, kWhereOFull = 7, kWhereDrain = 8;
 // index checks of the debug build (dev_check): Q tile, K/V tile, tensor
 // memory columns, output row store, LSE store
-constexpr int kChkQTile = 0x11, kChkKvTile = 0x12, kChkTmem = 0x13, kChkStore = 0x14, kChkLse = 0x15;
+constexpr int kChkQTile = 0x11, kChkKvTile = 0x12, kChkTmem = 0x13, kChkStore = 0x14, kChkLse = 0x15,
+              kChkUnit = 0x16;
 
 struct Params {
     __nv_bfloat16 *o;
@@ -121,6 +126,10 @@ struct Params {
     // of chunks within window_chunks of its own, plus the first and the last
     // frame; queries in the first and the last frame see every key.
     int frame_tokens, chunk_frames, window_chunks;
+    // windowed attention: the units of CTA b are sched[b * sched_ld + i],
+    // i = 0, 1, ... up to a -1 (unit = head offset * q_blocks + q-block)
+    const int *sched;
+    int sched_ld;
 };
 
 // The K/V tiles one work unit visits: up to three ascending, disjoint ranges
@@ -128,7 +137,7 @@ struct Params {
 struct KvList {
     int lo[3], hi[3];
     int count;
-    __device__ __forceinline__ int tile(int idx) const {
+    __host__ __device__ __forceinline__ int tile(int idx) const {
         const int n0 = hi[0] - lo[0];
         if (idx < n0) return lo[0] + idx;
         idx -= n0;
@@ -158,28 +167,29 @@ __device__ __forceinline__ RowWindow row_window(const Params &p, int row) {
     return r;
 }
 
-template <bool kWindow>
-__device__ __forceinline__ KvList kv_list(const Params &p, int qb) {
+// The K/V tiles of windowed q-block qb (n tokens, kv_tiles tiles of 128,
+// frames of T tokens in chunks of C frames, W chunks either side).
+__host__ __device__ inline KvList window_kv_list(int n, int kv_tiles, int T, int C, int W, int qb) {
     KvList L;
     L.lo[0] = 0;
-    L.hi[0] = p.kv_tiles;
+    L.hi[0] = kv_tiles;
     L.lo[1] = L.hi[1] = L.lo[2] = L.hi[2] = 0;
-    L.count = p.kv_tiles;
-    if (!kWindow) return L;
-    const int T = p.frame_tokens, C = p.chunk_frames, frames = frames_of(p);
+    L.count = kv_tiles;
+    const int frames = n / T;
     const int r0 = qb * kUnitRows;
-    const int r1 = min(p.n, r0 + kUnitRows);
+    const int r1 = n < r0 + kUnitRows ? n : r0 + kUnitRows;
     const int f0 = r0 / T, f1 = (r1 - 1) / T;
     if (f0 == 0 || f1 >= frames - 1) return L;  // an anchor row: every key
     // key tokens: first frame, the union of the rows' windows, last frame
+    const int w_lo = (f0 / C - W) * C, w_hi = (f1 / C + W + 1) * C;
     const int x[3][2] = {{0, T},
-                         {max(0, (f0 / C - p.window_chunks) * C) * T, min(frames, (f1 / C + p.window_chunks + 1) * C) * T},
-                         {(frames - 1) * T, p.n}};
+                         {(w_lo > 0 ? w_lo : 0) * T, (w_hi < frames ? w_hi : frames) * T},
+                         {(frames - 1) * T, n}};
     int m = 0;
     for (int r = 0; r < 3; ++r) {
         const int lo = x[r][0] / kRows, hi = (x[r][1] + kRows - 1) / kRows;
         if (m > 0 && lo <= L.hi[m - 1]) {
-            L.hi[m - 1] = max(L.hi[m - 1], hi);
+            L.hi[m - 1] = L.hi[m - 1] > hi ? L.hi[m - 1] : hi;
         } else {
             L.lo[m] = lo;
             L.hi[m] = hi;
@@ -191,13 +201,23 @@ __device__ __forceinline__ KvList kv_list(const Params &p, int qb) {
     return L;
 }
 
+template <bool kWindow>
+__device__ __forceinline__ KvList kv_list(const Params &p, int qb) {
+    if (kWindow) return window_kv_list(p.n, p.kv_tiles, p.frame_tokens, p.chunk_frames, p.window_chunks, qb);
+    KvList L;
+    L.lo[0] = 0;
+    L.hi[0] = p.kv_tiles;
+    L.lo[1] = L.hi[1] = L.lo[2] = L.hi[2] = 0;
+    L.count = p.kv_tiles;
+    return L;
+}
+
 // The i-th work unit of this CTA, as (head offset, q-block); false past the
 // last one.  Dense attention: units dealt round-robin, heads outermost (all
-// units cost the same).  Windowed attention: the q-blocks holding a row of
-// the first or the last frame see every key and cost several times more, so
-// they come first (one per CTA at most, for a launch of <= grid of them), the
-// others follow in their usual order, and the deal runs in snake order
-// (alternating direction every wave) so that the CTAs' totals even out.
+// units cost the same).  Windowed attention: units cost their K/V tile count
+// (a q-block holding a row of the first or the last frame sees every key),
+// and the host deals them longest first, each to the CTA with the least work
+// so far (the table in sched), so that the CTAs' totals even out.
 template <bool kWindow>
 __device__ __forceinline__ bool unit_at(const Params &p, int i, int &head_off, int &qb) {
     const int grid = (int)gridDim.x, b = (int)blockIdx.x;
@@ -208,23 +228,11 @@ __device__ __forceinline__ bool unit_at(const Params &p, int i, int &head_off, i
         qb = u % p.q_blocks;
         return true;
     }
-    const int u = i * grid + ((i & 1) ? grid - 1 - b : b);
-    if (u >= p.num_units) return false;
-    const int heads = p.num_units / p.q_blocks;
-    const int T = p.frame_tokens, frames = frames_of(p);
-    const int a0 = min(p.q_blocks, (T + kUnitRows - 1) / kUnitRows);     // q-blocks touching frame 0
-    const int b1 = max(a0, ((frames - 1) * T) / kUnitRows);               // first q-block touching frame F-1
-    const int na = a0 + (p.q_blocks - b1);                                // anchor q-blocks per head
-    if (u < heads * na) {
-        head_off = u / na;
-        const int a = u % na;
-        qb = a < a0 ? a : b1 + (a - a0);
-    } else {
-        const int nn = p.q_blocks - na;
-        const int j = u - heads * na;
-        head_off = j / nn;
-        qb = a0 + j % nn;
-    }
+    if (!dev_check(i < p.sched_ld, p.status, kChkUnit)) return false;
+    const int u = p.sched[(size_t)b * (size_t)p.sched_ld + (size_t)i];
+    if (u < 0) return false;
+    head_off = u / p.q_blocks;
+    qb = u % p.q_blocks;
     return true;
 }
 
@@ -758,6 +766,69 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t n, int ld) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Windowed launches: the deal of units to CTAs.  A unit costs its K/V tile
+// count; units go longest first, each to the CTA with the least work so far,
+// and each CTA then runs its units in (head, q-block) order, so the CTAs
+// running at the same time read neighbouring keys.  One table per geometry
+// (grid x ld ints, a few KB), built on first use and kept for the library's
+// lifetime.
+struct SchedKey {
+    int64_t n;
+    int frame_tokens, chunk_frames, window_chunks, heads, grid, dev;
+    bool operator==(const SchedKey &o) const {
+        return n == o.n && frame_tokens == o.frame_tokens && chunk_frames == o.chunk_frames &&
+               window_chunks == o.window_chunks && heads == o.heads && grid == o.grid && dev == o.dev;
+    }
+};
+
+fv_status window_schedule(const SchedKey &k, int q_blocks, int kv_tiles, const int **table, int *ld) {
+    static std::mutex mu;
+    static std::vector<std::pair<SchedKey, std::pair<int *, int>>> cache;
+    std::lock_guard<std::mutex> g(mu);
+    for (const auto &e : cache)
+        if (e.first == k) {
+            *table = e.second.first;
+            *ld = e.second.second;
+            return FV_OK;
+        }
+    const int units = k.heads * q_blocks;
+    std::vector<int> cost(q_blocks);
+    for (int qb = 0; qb < q_blocks; ++qb)
+        cost[qb] = window_kv_list((int)k.n, kv_tiles, k.frame_tokens, k.chunk_frames, k.window_chunks, qb).count;
+    std::vector<int> order(units);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int a, int b) { return cost[a % q_blocks] > cost[b % q_blocks]; });
+    std::vector<std::vector<int>> lists(k.grid);
+    using Load = std::pair<int64_t, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
+    for (int c = 0; c < k.grid; ++c) least.push({0, c});
+    for (int u : order) {
+        const Load l = least.top();
+        least.pop();
+        lists[l.second].push_back(u);
+        least.push({l.first + cost[u % q_blocks], l.second});
+    }
+    size_t longest = 0;
+    for (auto &l : lists) {
+        std::sort(l.begin(), l.end());
+        longest = std::max(longest, l.size());
+    }
+    const int width = (int)longest + 1;   // room for the -1 that ends every list
+    std::vector<int> host((size_t)k.grid * width, -1);
+    for (int c = 0; c < k.grid; ++c) std::copy(lists[c].begin(), lists[c].end(), host.begin() + (size_t)c * width);
+    int *dev = nullptr;
+    if (cudaMalloc(&dev, host.size() * sizeof(int)) != cudaSuccess) return FV_ERR_LAUNCH;
+    if (cudaMemcpy(dev, host.data(), host.size() * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaFree(dev);
+        return FV_ERR_LAUNCH;
+    }
+    cache.push_back({k, {dev, width}});
+    *table = dev;
+    *ld = width;
+    return FV_OK;
+}
+
 }  // namespace
 
 EncodeTiledFn tensor_map_encoder() {
@@ -812,6 +883,13 @@ fv_status launch_attn_fwd(const AttnLaunch &a, cudaStream_t stream) {
     p.chunk_frames = a.chunk_frames;
     p.window_chunks = a.window_chunks;
     const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
+    p.sched = nullptr;
+    p.sched_ld = 0;
+    if (a.frame_tokens > 0) {
+        const SchedKey key{a.n, a.frame_tokens, a.chunk_frames, a.window_chunks, a.heads, grid, dev};
+        const fv_status st = window_schedule(key, p.q_blocks, p.kv_tiles, &p.sched, &p.sched_ld);
+        if (st != FV_OK) return st;
+    }
     if (a.frame_tokens > 0)
         attn_fwd_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
     else
