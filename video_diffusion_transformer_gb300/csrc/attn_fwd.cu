@@ -10,8 +10,9 @@
 //
 // Design (one persistent CTA per SM, 384 threads):
 //   * work unit = (head, block of 256 query rows) = two 128-row q-tiles;
-//     units are dealt round-robin, heads outermost, so the CTAs running at
-//     the same time stream the same head's K/V through L2;
+//     dense units are dealt round-robin, heads outermost, so the CTAs
+//     running at the same time stream the same head's K/V through L2
+//     (windowed units, of unequal cost, from a longest-first table);
 //   * warp 8 (one thread) issues TMA loads: the two Q tiles of a unit, then
 //     K_0, V_0, K_1, V_1, ... into a 4-slot ring of 32 KB tiles, each tile two
 //     128 x 64 bf16 halves in the 128-byte swizzled layout;
@@ -105,7 +106,7 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr int kWhereQEmpty = 1, kWhereKvEmpty = 2, kWhereQFull = 3, kWhereKvFull = 4, kWherePFull = 5,
               kWhereSFull = 6, kWhereOFull = 7, kWhereDrain = 8;
 // index checks of the debug build (dev_check): Q tile, K/V tile, tensor
-// memory columns, output row store, LSE store
+// memory columns, output row store, LSE store, windowed unit table
 constexpr int kChkQTile = 0x11, kChkKvTile = 0x12, kChkTmem = 0x13, kChkStore = 0x14, kChkLse = 0x15,
               kChkUnit = 0x16;
 
