@@ -124,6 +124,14 @@ fv_status fv_attn_fwd(const void *Q, const void *K, const void *V, void *O,
  * window_chunks >= 0; otherwise FV_ERR_SHAPE.  The model's values are
  * frame_tokens = (H/32)(W/32) (1,008 at 1344x768), chunk_frames = 5,
  * window_chunks = 1.  All other arguments as fv_attn_fwd.
+ *
+ * Memory: query blocks differ in cost (the anchors' see every key), so each
+ * launch deals them to the CTAs from a table the library builds on the host
+ * on the first call with a given geometry (N, frame_tokens, chunk_frames,
+ * window_chunks, heads per launch, device), copies to a small device buffer
+ * (grid x longest list ints, a few KB; cudaMalloc and a synchronous
+ * cudaMemcpy) and keeps for the library's lifetime.  Later calls with the
+ * same geometry allocate nothing.
  */
 fv_status fv_attn_fwd_window(const void *Q, const void *K, const void *V, void *O,
                              int64_t N, int H, int D, float scale, int head_group,
