@@ -556,9 +556,9 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
         }
         float m_used = -INFINITY, l = 0.f;
         for (int j = 0; j < n_kv; ++j) {
-            ok = __all_sync(0xffffffffu, wait_bar(sm, kBarSFull + k, tile & 1u, p, kWhereSFull));
-            if (!ok) break;
-            ptx::tc_fence_after();
+            // What the rows see of tile j depends only on j: worked out, votes
+            // included, before the scores are ready, so none of it sits
+            // between S and its probabilities.
             const int kb = (kWindow ? kl.tile(j) : j) * kRows;
             dev_check(kb >= 0 && kb < p.n && (t >> 5) < 4, p.status, kChkKvTile);
             ColMask<kWindow> cm;
@@ -569,7 +569,18 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
             cm.w1 = rw.w1 - kb;
             cm.a1 = last_begin - kb;
             const bool row_none = cm.none();
-            if (kWindow && __all_sync(0xffffffffu, row_none)) {
+            const bool warp_none = kWindow && __all_sync(0xffffffffu, row_none);
+            // A row sees all of the tile, none of it, or part of it.  Only a
+            // partly visible row needs the per-column test; a row that sees
+            // none gets an infinite offset, so its probabilities are exact zeros.
+            const bool row_full = cm.valid >= kRows &&
+                                  (!kWindow || cm.all || (cm.w0 <= 0 && cm.w1 >= kRows) || cm.a0 >= kRows || cm.a1 <= 0);
+            // one code path per warp: the tcgen05 copies are warp-collective
+            const bool masked = __any_sync(0xffffffffu, !row_full && !row_none);
+            ok = __all_sync(0xffffffffu, wait_bar(sm, kBarSFull + k, tile & 1u, p, kWhereSFull));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            if (warp_none) {
                 // No row of this warp sees any key of the tile: zero probabilities,
                 // no scores read (never the first tile, which holds the first frame).
                 uint32_t zero[16];
@@ -589,13 +600,6 @@ __device__ void softmax_role(const Params &p, const Smem &sm, uint32_t tmem, int
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) ptx::reg_fence(s[c4]);
-            // A row sees all of the tile, none of it, or part of it.  Only a
-            // partly visible row needs the per-column test; a row that sees
-            // none gets an infinite offset, so its probabilities are exact zeros.
-            const bool row_full = cm.valid >= kRows &&
-                                  (!kWindow || cm.all || (cm.w0 <= 0 && cm.w1 >= kRows) || cm.a0 >= kRows || cm.a1 <= 0);
-            // one code path per warp: the tcgen05 copies are warp-collective
-            const bool masked = __any_sync(0xffffffffu, !row_full && !row_none);
             // The reference maximum m_used is the first tile's row maximum; later
             // tiles exponentiate against it directly (no per-tile maximum on the
             // critical path) and only a tile whose probabilities sum above 2^20
