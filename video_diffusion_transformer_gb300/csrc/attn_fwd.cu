@@ -169,7 +169,10 @@ __device__ __forceinline__ RowWindow row_window(const Params &p, int row) {
 }
 
 // The K/V tiles of windowed q-block qb (n tokens, kv_tiles tiles of 128,
-// frames of T tokens in chunks of C frames, W chunks either side).
+// frames of T tokens in chunks of C frames, W chunks either side).  The
+// three ranges (first frame, window, last frame) are ascending; overlapping
+// or touching ones merge.  Written with constant indices only, so the list
+// stays in registers.
 __host__ __device__ inline KvList window_kv_list(int n, int kv_tiles, int T, int C, int W, int qb) {
     KvList L;
     L.lo[0] = 0;
@@ -183,22 +186,33 @@ __host__ __device__ inline KvList window_kv_list(int n, int kv_tiles, int T, int
     if (f0 == 0 || f1 >= frames - 1) return L;  // an anchor row: every key
     // key tokens: first frame, the union of the rows' windows, last frame
     const int w_lo = (f0 / C - W) * C, w_hi = (f1 / C + W + 1) * C;
-    const int x[3][2] = {{0, T},
-                         {(w_lo > 0 ? w_lo : 0) * T, (w_hi < frames ? w_hi : frames) * T},
-                         {(frames - 1) * T, n}};
-    int m = 0;
-    for (int r = 0; r < 3; ++r) {
-        const int lo = x[r][0] / kRows, hi = (x[r][1] + kRows - 1) / kRows;
-        if (m > 0 && lo <= L.hi[m - 1]) {
-            L.hi[m - 1] = L.hi[m - 1] > hi ? L.hi[m - 1] : hi;
+    const int t1 = (w_lo > 0 ? w_lo : 0) * T, t2 = (w_hi < frames ? w_hi : frames) * T;
+    const int a0 = 0, b0 = (T + kRows - 1) / kRows;
+    const int a1 = t1 / kRows, b1 = (t2 + kRows - 1) / kRows;
+    const int a2 = ((frames - 1) * T) / kRows, b2 = (n + kRows - 1) / kRows;
+    int lo0 = a0, hi0 = b0, lo1 = 0, hi1 = 0, lo2 = 0, hi2 = 0;
+    if (a1 <= hi0) {
+        hi0 = hi0 > b1 ? hi0 : b1;
+        if (a2 <= hi0) {
+            hi0 = hi0 > b2 ? hi0 : b2;
         } else {
-            L.lo[m] = lo;
-            L.hi[m] = hi;
-            ++m;
+            lo1 = a2;
+            hi1 = b2;
+        }
+    } else {
+        lo1 = a1;
+        hi1 = b1;
+        if (a2 <= hi1) {
+            hi1 = hi1 > b2 ? hi1 : b2;
+        } else {
+            lo2 = a2;
+            hi2 = b2;
         }
     }
-    for (int r = m; r < 3; ++r) L.lo[r] = L.hi[r] = 0;
-    L.count = (L.hi[0] - L.lo[0]) + (L.hi[1] - L.lo[1]) + (L.hi[2] - L.lo[2]);
+    L.lo[0] = lo0, L.hi[0] = hi0;
+    L.lo[1] = lo1, L.hi[1] = hi1;
+    L.lo[2] = lo2, L.hi[2] = hi2;
+    L.count = (hi0 - lo0) + (hi1 - lo1) + (hi2 - lo2);
     return L;
 }
 
